@@ -1,0 +1,259 @@
+/*
+ * libpagedattn -- attention over a paged KV cache on one NVIDIA GB300 (sm_103a).
+ *
+ * Plain C ABI.  Every pointer argument is a DEVICE pointer unless it is
+ * marked "host"; sizes are in elements unless marked "bytes".  The caller
+ * owns every buffer (inputs, caches, outputs, workspace); the library
+ * allocates no device memory.  Every call validates its arguments on the host
+ * first: on a non-OK status nothing has been enqueued.  On PA_OK the work is
+ * enqueued on `stream` and runs asynchronously; a later device-side problem
+ * (an out-of-range page id or slot the host could not see) is never turned
+ * into an out-of-bounds access -- the kernel skips the access and raises a
+ * flag that pa_read_device_errors() returns.
+ *
+ * Cache layout (nano-vLLM learning note, allocate_kv_cache listing):
+ *   k_cache, v_cache: [num_pages, page_size, num_kv_heads, head_dim], row-major.
+ *   Flat slot s = page * page_size + offset holds one token's
+ *   num_kv_heads * head_dim elements.
+ * Query-head grouping (nano-vLLM learning note, Qwen3Attention.forward
+ * listing): q-head h reads kv-head h / (num_q_heads / num_kv_heads).
+ *
+ * Supported: dtype fp32 or bf16; head_dim 64 or 128; num_kv_heads a power of
+ * two <= 8; group size num_q_heads / num_kv_heads in 1..8; page_size a power
+ * of two >= 16.  All vector pointers and row strides must be 16-byte aligned.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* The library is built with hidden visibility; only these entry points are exported. */
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,        /* a required pointer is NULL */
+  PA_ERR_DTYPE = 2,       /* dtype is neither PA_F32 nor PA_BF16 */
+  PA_ERR_SHAPE = 3,       /* a count, size or stride is out of range */
+  PA_ERR_ALIGN = 4,       /* a pointer or row stride is not 16-byte aligned */
+  PA_ERR_UNSUPPORTED = 5, /* well-formed but outside the supported set */
+  PA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required */
+  PA_ERR_CUDA = 7,        /* a CUDA call or launch failed (pa_last_cuda_error) */
+  PA_ERR_VALIDATION = 8   /* reserved for callers of pa_validate_metadata */
+} pa_status;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Shape of one layer's cache and of the attention heads that read it. */
+typedef struct pa_cache_desc {
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int64_t num_pages;
+  int32_t dtype; /* pa_dtype */
+} pa_cache_desc;
+
+/* A cudaStream_t passed as an opaque pointer; NULL is the legacy default stream. */
+typedef void* pa_stream_t;
+
+/* Device-side flags returned by pa_read_device_errors(). */
+#define PA_DEVERR_BAD_SLOT 0x1u     /* a slot outside [-1, num_pages*page_size) was skipped */
+#define PA_DEVERR_BAD_PAGE 0x2u     /* a block-table entry outside [0, num_pages) was skipped */
+#define PA_DEVERR_BAD_LENGTH 0x4u   /* a context / chunk length was inconsistent; request skipped */
+#define PA_DEVERR_TIMEOUT 0x8u      /* a bounded wait on an async copy gave up; output invalid */
+
+/*
+ * pa_slot_mapping -- positions and physical slots of each request's new tokens.
+ *
+ * Defined by the nano-vLLM learning note's prepare_prefill listing (new tokens
+ * of a request sit at positions num_cached .. num_cached + num_new - 1) and
+ * prepare_decode listing (slot = block_table[pos / page_size] * page_size +
+ * pos % page_size).
+ *
+ *   batch            requests B (host).
+ *   cu_seqlens_q     int32 [B+1], 0 = cu[0] <= cu[1] <= ... ; request b's new
+ *                    tokens are rows cu[b] .. cu[b+1]-1 of the packed batch.
+ *                    Decode is the case cu = 0, 1, ..., B.
+ *   context_lens     int32 [B], tokens of request b INCLUDING its new ones.
+ *   block_tables     int32 [B, max_pages_per_seq], physical page ids.
+ *   num_tokens       cu[B] (host).
+ *   positions        int32 [num_tokens] out: context_lens[b] - n_b + j.
+ *   slot_mapping     int64 [num_tokens] out; -1 (and PA_DEVERR_* raised) for a
+ *                    token whose page entry is out of range.
+ */
+PA_API pa_status pa_slot_mapping(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
+                          const int32_t* context_lens, const int32_t* block_tables,
+                          int32_t max_pages_per_seq, int64_t num_tokens, int32_t* positions,
+                          int64_t* slot_mapping, pa_stream_t stream);
+
+/*
+ * pa_kv_write -- scatter each new token's K and V row into its cache slot.
+ *
+ * Defined by the nano-vLLM learning note's store_kvcache_kernel listing: row t
+ * of k (v) is copied bit for bit to flat slot slot_mapping[t] of k_cache
+ * (v_cache); slot -1 stores nothing.
+ *
+ *   k, v             [num_tokens, num_kv_heads, head_dim] rows, row t at
+ *                    k + t * k_row_stride (elements, >= num_kv_heads*head_dim,
+ *                    a multiple of 16 bytes).  May be views into a fused qkv.
+ *   slot_mapping     int64 [num_tokens]; entries outside [-1, num_pages *
+ *                    page_size) are skipped and flagged PA_DEVERR_BAD_SLOT.
+ *   k_cache, v_cache caches as described at the top of this file.
+ */
+PA_API pa_status pa_kv_write(const pa_cache_desc* desc, const void* k, int64_t k_row_stride,
+                      const void* v, int64_t v_row_stride, int64_t num_tokens,
+                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                      pa_stream_t stream);
+
+/*
+ * pa_qk_norm_rope_kv_write -- per-head RMSNorm of q and k, rotary embedding of
+ * both at absolute positions, then the KV write of (k, v).
+ *
+ * Defined by the nano-vLLM learning note: RMSNorm.rms_forward listing (mean of
+ * squares in fp32, x * rsqrt(mean + eps) cast back to the dtype, then times
+ * the weight), apply_rotary_emb and inv_freq listings (half-split rotation,
+ * frequency theta^(-2i/head_dim), evaluated in fp32 and cast back), and the
+ * Qwen3Attention.forward listing for the order (norm, rotary, store, attend).
+ *
+ *   q                [num_tokens, num_q_heads, head_dim] rows at q_row_stride.
+ *   k, v             rows at k_row_stride / v_row_stride (as pa_kv_write).
+ *   positions        int32 [num_tokens], absolute positions (pa_slot_mapping).
+ *   q_norm_w, k_norm_w  [head_dim] weights in the cache dtype.
+ *   eps, rope_theta  RMSNorm epsilon and rotary base (host).
+ *   q_out            [num_tokens, num_q_heads, head_dim] contiguous output; it
+ *                    may equal q only when q_row_stride == num_q_heads*head_dim.
+ *   slot_mapping     as pa_kv_write; the normed, rotated k and the unchanged v
+ *                    are written there.
+ */
+PA_API pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride,
+                                   const void* k, int64_t k_row_stride, const void* v,
+                                   int64_t v_row_stride, int64_t num_tokens,
+                                   const int32_t* positions, const void* q_norm_w,
+                                   const void* k_norm_w, float eps, float rope_theta,
+                                   const int64_t* slot_mapping, void* q_out, void* k_cache,
+                                   void* v_cache, pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * these host-side sizes on the CURRENT device (the split plan depends on its SM
+ * count).  max_ctas: 0 for the library's choice, else an upper bound on the
+ * number of key-range partitions.  Returns 0 on an invalid descriptor or when no
+ * CUDA device is usable.
+ */
+PA_API size_t pa_decode_workspace_size(const pa_cache_desc* desc, int32_t batch, int32_t max_context_len,
+                                int32_t max_ctas);
+
+/*
+ * pa_decode_plan_info -- how pa_decode would split this batch on the CURRENT
+ * device (host outs, either may be NULL): the number of key-range partitions
+ * (CTAs; a merge kernel runs when it is above 1) and the tokens per chunk that
+ * one pipeline stage moves.  Same arguments and failure cases as
+ * pa_decode_workspace_size.
+ */
+PA_API pa_status pa_decode_plan_info(const pa_cache_desc* desc, int32_t batch, int32_t max_context_len,
+                                     int32_t max_ctas, int32_t* num_partitions, int32_t* tokens_per_chunk);
+
+/*
+ * pa_decode -- batched GQA decode attention over the paged cache.
+ *
+ * For each request b and q-head h: out[b, h] = sum_j softmax_j(scale * q[b,h] .
+ * K_j) V_j over the request's keys j < context_lens[b], found through
+ * block_tables[b] (nano-vLLM learning note, Attention.forward listing: decode
+ * attends to the cache after the step's KV write; prepare_decode listing:
+ * context_lens counts the new token).
+ *
+ * The keys of all requests are cut into equal shares, one per CTA; a request
+ * spread over several CTAs gets per-share (o, log-sum-exp) partials that a
+ * second kernel merges (split-KV).  Shares depend only on context_lens, so the
+ * result is bitwise independent of which physical pages hold the keys.
+ *
+ *   q                [batch, num_q_heads, head_dim] contiguous.
+ *   block_tables     int32 [batch, max_pages_per_seq].
+ *   context_lens     int32 [batch], each in [1, max_context_len]; a request
+ *                    outside that range is skipped (its output untouched) and
+ *                    flagged PA_DEVERR_BAD_LENGTH.
+ *   max_context_len  host upper bound on context_lens (sizes the split plan).
+ *   scale            softmax scale (host), e.g. 1/sqrt(head_dim).
+ *   max_ctas         0 = library choice; else at most this many partitions
+ *                    (1 = no split).
+ *   out              [batch, num_q_heads, head_dim] contiguous, cache dtype.
+ *   workspace        >= pa_decode_workspace_size(...) bytes, 256-byte aligned;
+ *                    no initialisation needed; not shared with a concurrent call.
+ */
+PA_API pa_status pa_decode(const pa_cache_desc* desc, const void* q, int32_t batch, const void* k_cache,
+                    const void* v_cache, const int32_t* block_tables, int32_t max_pages_per_seq,
+                    const int32_t* context_lens, int32_t max_context_len, float scale,
+                    int32_t max_ctas, void* out, void* workspace, size_t workspace_bytes,
+                    pa_stream_t stream);
+
+/*
+ * pa_prefill_varlen -- chunked-prefill attention for packed new tokens.
+ *
+ * Request b's chunk is rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q (flat
+ * varlen packing, qwen-engine README); those n_b tokens are the last n_b of its
+ * context_lens[b] tokens, so row i sits at position context_lens[b] - n_b + i
+ * and attends to keys 0 .. that position: the cached prefix plus the causal
+ * part of its own chunk, all read from the cache (nano-vLLM learning note,
+ * Attention.forward listing: with block tables, k and v come from the cache
+ * after the step's KV write).
+ *
+ *   q                [num_tokens, num_q_heads, head_dim] contiguous (already
+ *                    normed and rotated, e.g. q_out of pa_qk_norm_rope_kv_write).
+ *   cu_seqlens_q     int32 [batch+1] as in pa_slot_mapping; num_tokens = cu[batch].
+ *   max_seqlen_q     host upper bound on n_b.
+ *   context_lens     int32 [batch], n_b <= context_lens[b] <= max_context_len.
+ *   out              [num_tokens, num_q_heads, head_dim] contiguous.
+ * bf16 with head_dim 128 runs on the tcgen05 tensor cores; other cases on a
+ * CUDA-core kernel.
+ */
+PA_API pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q,
+                            int32_t batch, int32_t max_seqlen_q, int64_t num_tokens,
+                            const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int32_t max_pages_per_seq, const int32_t* context_lens,
+                            int32_t max_context_len, float scale, void* out, pa_stream_t stream);
+
+/*
+ * pa_validate_metadata -- opt-in device check of the metadata the other calls
+ * trust.  Counts, into *error_count (device int32, overwritten), the requests
+ * with context_lens outside [1, min(max_context_len, max_pages_per_seq *
+ * page_size)], new-token counts that are negative or exceed the context (when
+ * cu_seqlens_q is given; may be NULL), and block-table entries outside
+ * [0, num_pages) among the pages a request uses.  Never faults; read the count
+ * after synchronising.
+ */
+PA_API pa_status pa_validate_metadata(const pa_cache_desc* desc, int32_t batch,
+                               const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                               const int32_t* block_tables, int32_t max_pages_per_seq,
+                               int32_t max_context_len, int32_t* error_count, pa_stream_t stream);
+
+/*
+ * pa_read_device_errors -- the PA_DEVERR_* flags raised on the current device
+ * since the last reset (host out).  Synchronises the device.  reset != 0
+ * clears the flags.
+ */
+PA_API pa_status pa_read_device_errors(uint32_t* flags, int32_t reset);
+
+/* CUDA error code behind the calling thread's last PA_ERR_CUDA (0 if none). */
+PA_API int32_t pa_last_cuda_error(void);
+
+/* Static description of a status code. */
+PA_API const char* pa_status_string(pa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PA_API int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

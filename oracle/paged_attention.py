@@ -361,14 +361,15 @@ def within_tolerance(got, ref, dtype: str):
     return bool(np.isfinite(err) and err <= bound), err, bound
 
 
-def reference_step(wl, requests: Optional[Sequence[int]] = None):
+def reference_step(wl, requests: Optional[Sequence[int]] = None, with_attention: bool = True):
     """One whole step of a workload, computed by the oracle from the seeded inputs.
 
     Builds the cache from the history rows with the oracle's own slot mapping
     and KV write, applies the step's own norm/rotation (if the workload has
     norm weights) and KV write, then attends.  Returns a dict with the caches,
     the new tokens' positions / slots, the q actually attended (storage) and
-    the float64 outputs of the selected requests.
+    the float64 outputs of the selected requests (None when
+    ``with_attention`` is False).
     """
     dt = wl.dtype
     k_cache = wl.poison_storage(wl.cache_shape())
@@ -381,7 +382,9 @@ def reference_step(wl, requests: Optional[Sequence[int]] = None):
         q, k = qk_norm_rope(wl.q, wl.k_new, wl.q_norm_w, wl.k_norm_w, positions,
                             wl.eps, wl.rope_theta, dt)
     kv_write(k, wl.v_new, slots, k_cache, v_cache)
-    if wl.kind == "decode":
+    if not with_attention:
+        o = lse = None
+    elif wl.kind == "decode":
         o, lse = decode(q, k_cache, v_cache, wl.block_tables, wl.context_lens, wl.scale, dt, requests)
     else:
         o, lse = prefill(q, wl.cu_seqlens_q, k_cache, v_cache, wl.block_tables, wl.context_lens,

@@ -1,0 +1,698 @@
+// Batched GQA decode attention over a paged KV cache (sm_103a).
+//
+// Semantics (nano-vLLM learning note, Attention.forward and prepare_decode
+// listings): each request's single query attends to all context_lens[b] keys
+// of its block table, after this step's KV write.
+//
+// Design (HBM-bound):
+//   * The keys of all requests are cut into chunks of T tokens (T divides the
+//     page size, so a chunk lies inside one page and is one contiguous run of
+//     T * Hkv * head_dim elements).  The global chunk list is split evenly
+//     over the CTAs of one wave ("plan" kernel), so every SM streams the same
+//     number of bytes whatever the length mix.  A request cut across CTAs
+//     gets per-CTA (o, log2-sum-exp) partials, merged by a second kernel
+//     (split-KV / flash-decoding).  The cut depends only on context_lens, so
+//     results are bitwise independent of physical page ids.
+//   * One producer warp issues 1-D bulk async copies (TMA engine) of each
+//     chunk's K and V rows into a 3-stage shared-memory ring, with mbarrier
+//     completion and an evict-first L2 hint.  Its 32 lanes look up block-table
+//     entries for 32 chunks at a time.
+//   * One consumer warp per kv-head reads its head's rows of the chunk: each
+//     lane owns 16 bytes of a row, so one K/V byte feeds all G q-heads of the
+//     group from registers.  Dot products use packed fp32x2 FMA; partial sums
+//     are reduced with a halving butterfly of warp shuffles; the online
+//     softmax runs in base 2 with the scale folded into q.
+//   * Every wait is bounded (pa::mbar_wait_bounded): a kernel never hangs.
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTPL = 4;          // tokens per lane per chunk
+constexpr int kStages = 3;       // shared-memory ring depth
+constexpr int kPlanThreads = 1024;
+constexpr int kMergeThreads = 256;
+
+__host__ __device__ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
+__host__ __device__ constexpr int pow2ceil(int x) { return x <= 1 ? 1 : 2 * pow2ceil((x + 1) / 2); }
+
+template <typename T, int HD>
+struct Geom {
+  static constexpr int E = sizeof(T);
+  static constexpr int DPL = 16 / E;      // elements a lane holds of one row
+  static constexpr int NPR = DPL / 2;     // float2 pairs per lane
+  static constexpr int LPR = HD / DPL;    // lanes covering one head row
+  static constexpr int RPI = 32 / LPR;    // rows one warp instruction covers
+  static constexpr int TOK = kTPL * RPI;  // tokens per chunk
+  static constexpr int RB = HD * E;       // bytes of one head row
+};
+
+struct KParams {
+  const char* q;
+  const char* k_cache;
+  const char* v_cache;
+  const int32_t* bt;
+  const int32_t* ctx;
+  char* out;
+  float* o_part;
+  float* lse_part;
+  int32_t* cs;       // [B+1] chunk prefix sums
+  int32_t* cta_seq;  // [n_ctas] first request of each CTA
+  unsigned int* err;
+  int64_t num_pages;
+  int32_t B, Hq, Hkv, P, maxp, max_ctx, n_ctas;
+  int32_t log2P, log2T;
+  int32_t row_bytes;    // Hkv * HD * E, one token of the cache
+  int32_t chunk_bytes;  // T * row_bytes
+  uint32_t off_bar, off_meta, off_p, off_alpha, off_ml, off_abort;
+  int32_t p_row;        // floats per token row of the probability tile
+  float scale_log2;     // softmax scale * log2(e)
+};
+
+// ---------------------------------------------------------------------------
+// plan: chunk prefix sums and each CTA's first request
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams p) {
+  __shared__ int32_t warp_tot[kPlanThreads / 32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x;
+  const int T = 1 << p.log2T;
+  const int cap = min(p.max_ctx, p.maxp << p.log2P);
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < p.B; base += kPlanThreads) {
+    const int b = base + tid;
+    int cnt = 0;
+    if (b < p.B) {
+      const int L = p.ctx[b];
+      if (L >= 1 && L <= cap) {
+        cnt = (L + T - 1) >> p.log2T;
+      } else {
+        raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
+      }
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((tid & 31) >= o) x += y;
+    }
+    if ((tid & 31) == 31) warp_tot[tid >> 5] = x;
+    __syncthreads();
+    if (tid < 32) {
+      int w = warp_tot[tid];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (tid >= o) w += y;
+      }
+      warp_tot[tid] = w;
+    }
+    __syncthreads();
+    const int incl = x + ((tid >> 5) ? warp_tot[(tid >> 5) - 1] : 0) + carry;
+    if (b < p.B) p.cs[b + 1] = incl;
+    __syncthreads();
+    if (tid == kPlanThreads - 1) carry = incl;
+    __syncthreads();
+  }
+  if (tid == 0) p.cs[0] = 0;
+  __syncthreads();
+  const int NC = carry;
+  for (int c = tid; c < p.n_ctas; c += kPlanThreads) {
+    const int64_t x0 = (static_cast<int64_t>(c) * NC) / p.n_ctas;
+    int lo = 0, hi = p.B;  // first request whose chunks extend past x0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cs[mid + 1] > x0) hi = mid; else lo = mid + 1;
+    }
+    p.cta_seq[c] = lo;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// halving butterfly: reduce CUR values over the lanes of a row group, keeping
+// half of the (partially summed) values per step.
+// ---------------------------------------------------------------------------
+template <int CUR, int M>
+struct Butterfly {
+  template <int N>
+  static PA_DEVINL void run(float (&a)[N], int lane) {
+    if constexpr (CUR >= 2) {
+      constexpr int H = CUR / 2;
+      const bool upper = (lane & M) != 0;
+#pragma unroll
+      for (int u = 0; u < H; ++u) {
+        const float send = upper ? a[u] : a[u + H];
+        const float keep = upper ? a[u + H] : a[u];
+        a[u] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+      }
+      if constexpr (M > 1) Butterfly<H, M / 2>::run(a, lane);
+    } else {
+      a[0] += __shfl_xor_sync(0xffffffffu, a[0], M);
+      if constexpr (M > 1) Butterfly<1, M / 2>::run(a, lane);
+    }
+  }
+};
+
+template <typename T, int NPR>
+PA_DEVINL void unpack16(const uint4 w, float2 (&f)[NPR]) {
+  if constexpr (sizeof(T) == 2) {
+    f[0] = bf16x2_to_float2(w.x);
+    f[1] = bf16x2_to_float2(w.y);
+    f[2] = bf16x2_to_float2(w.z);
+    f[3] = bf16x2_to_float2(w.w);
+  } else {
+    f[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+    f[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+}
+
+template <typename T, int NPR>
+PA_DEVINL uint4 pack16(const float2 (&f)[NPR], float s) {
+  uint4 w;
+  if constexpr (sizeof(T) == 2) {
+    w.x = pack_bf16x2(f[0].x * s, f[0].y * s);
+    w.y = pack_bf16x2(f[1].x * s, f[1].y * s);
+    w.z = pack_bf16x2(f[2].x * s, f[2].y * s);
+    w.w = pack_bf16x2(f[3].x * s, f[3].y * s);
+  } else {
+    w.x = __float_as_uint(f[0].x * s);
+    w.y = __float_as_uint(f[0].y * s);
+    w.z = __float_as_uint(f[1].x * s);
+    w.w = __float_as_uint(f[1].y * s);
+  }
+  return w;
+}
+
+// Time-only bounded wait used when draining copies after an abort.
+PA_DEVINL void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the split-KV decode kernel
+// ---------------------------------------------------------------------------
+template <typename T, int HD, int G>
+__global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 112 : 168) decode_kernel(const KParams p) {
+  using Gm = Geom<T, HD>;
+  constexpr int LPR = Gm::LPR, RPI = Gm::RPI, NPR = Gm::NPR;
+  constexpr int V = G * kTPL;
+  constexpr int VP = pow2ceil(V);
+  constexpr int VF = VP >= LPR ? VP / LPR : 1;          // values a lane keeps
+  constexpr int DUP = VP >= LPR ? 0 : ilog2c(LPR / VP);  // low lane bits holding copies
+  constexpr int IBITS = ilog2c(kTPL / VF);               // lane bits carrying the token index
+  static_assert(VF <= kTPL, "a lane's values must share one head");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int c = blockIdx.x;
+  const int NW = p.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int NC = p.cs[p.B];
+  const int x0 = static_cast<int>((static_cast<int64_t>(c) * NC) / p.n_ctas);
+  const int x1 = static_cast<int>((static_cast<int64_t>(c + 1) * NC) / p.n_ctas);
+  if (x0 >= x1) return;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  uint64_t* empty = full + kStages;
+  int4* meta = reinterpret_cast<int4*>(smem + p.off_meta);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_abort);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ------------------------------ producer ------------------------------
+    const uint64_t pol = l2_policy_evict_first();
+    const int tok = 1 << p.log2T;
+    int b = p.cta_seq[c];
+    int issued = 0;
+    bool aborted = false;
+    for (int xg = x0; xg < x1 && !aborted; xg += 32) {
+      const int nvalid = min(32, x1 - xg);
+      const int x = xg + lane;
+      int my_b = b, n = 0, flags = 0;
+      long long off = 0;
+      if (lane < nvalid) {
+        while (my_b < p.B - 1 && p.cs[my_b + 1] <= x) ++my_b;
+        const int cb0 = p.cs[my_b], cb1 = p.cs[my_b + 1];
+        const int jc = x - cb0;
+        const int t0 = jc << p.log2T;
+        n = min(tok, p.ctx[my_b] - t0);
+        const int page = p.bt[static_cast<int64_t>(my_b) * p.maxp + (t0 >> p.log2P)];
+        if (page < 0 || page >= p.num_pages) {
+          raise_flag(p.err, PA_DEVERR_BAD_PAGE);
+          n = 0;
+        } else {
+          off = ((static_cast<long long>(page) << p.log2P) + (t0 & (p.P - 1))) * p.row_bytes;
+        }
+        flags = ((x == x0 || jc == 0) ? 1 : 0) | ((x == x1 - 1 || x == cb1 - 1) ? 2 : 0) |
+                ((cb0 >= x0 && cb1 <= x1) ? 4 : 0);
+      }
+      b = __shfl_sync(0xffffffffu, my_b, nvalid - 1);
+      for (int u = 0; u < nvalid; ++u) {
+        const int ub = __shfl_sync(0xffffffffu, my_b, u);
+        const int un = __shfl_sync(0xffffffffu, n, u);
+        const int uf = __shfl_sync(0xffffffffu, flags, u);
+        const long long uoff = __shfl_sync(0xffffffffu, off, u);
+        int ok = 1;
+        if (lane == 0) {
+          const int it = xg - x0 + u;
+          const int s = it % kStages;
+          if (!mbar_wait_bounded(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag, p.err)) {
+            ok = 0;
+          } else {
+            meta[s] = make_int4(ub, un, uf, 0);
+            const uint32_t bytes = static_cast<uint32_t>(un) * static_cast<uint32_t>(p.row_bytes);
+            mbar_arrive_expect_tx(&full[s], 2 * bytes);
+            if (bytes) {
+              unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
+              bulk_g2s_hint(dst, p.k_cache + uoff, bytes, &full[s], pol);
+              bulk_g2s_hint(dst + p.chunk_bytes, p.v_cache + uoff, bytes, &full[s], pol);
+            }
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          aborted = true;
+          break;
+        }
+      }
+    }
+    if (aborted && lane == 0) {
+      // Copies already issued may still be landing: wait for them (time only).
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        drain_wait(&full[it % kStages], (it / kStages) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------- consumers -------------------------------
+  const int h = warp;
+  const int rs = lane / LPR, j = lane % LPR;
+  const int vbase = (j >> DUP) * VF;
+  const int g_l = vbase / kTPL;          // head of the lane's kept values
+  const int i_l0 = vbase % kTPL;         // token index of its first kept value
+  const bool writer = (j & ((1 << DUP) - 1)) == 0;
+  const bool head_leader = writer && rs == 0 && (((j >> DUP) & ((1 << IBITS) - 1)) == 0) && g_l < G;
+  float* p_tile = reinterpret_cast<float*>(smem + p.off_p) + warp * Gm::TOK * p.p_row;
+  float* alpha_s = reinterpret_cast<float*>(smem + p.off_alpha) + warp * 8;
+  float* ml_s = reinterpret_cast<float*>(smem + p.off_ml) + warp * 16;
+
+  float2 qf[G][NPR];
+  float2 o[G][NPR];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  for (int x = x0, it = 0; x < x1; ++x, ++it) {
+    const int s = it % kStages;
+    if (!mbar_wait_bounded(&full[s], (it / kStages) & 1, abort_flag, p.err)) break;
+    const int4 md = meta[s];
+    const int b = md.x, n = md.y, flags = md.z;
+
+    if (flags & 1) {  // first chunk of this CTA's share of request b
+      const char* qb = p.q + (static_cast<int64_t>(b) * p.Hq + h * G) * Gm::RB + j * 16;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float2 f[NPR];
+        unpack16<T, NPR>(ldg16(qb + g * Gm::RB), f);
+#pragma unroll
+        for (int r = 0; r < NPR; ++r) {
+          qf[g][r] = make_float2(f[r].x * p.scale_log2, f[r].y * p.scale_log2);
+          o[g][r] = make_float2(0.f, 0.f);
+        }
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    const unsigned char* kbuf = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes + h * Gm::RB + j * 16;
+    const unsigned char* vbuf = kbuf + p.chunk_bytes;
+
+    // scores: partial dot products over this lane's 16 bytes of each row
+    float a[VP];
+#pragma unroll
+    for (int i = 0; i < kTPL; ++i) {
+      const int t = i * RPI + rs;
+      float2 kf[NPR];
+      unpack16<T, NPR>(*reinterpret_cast<const uint4*>(kbuf + t * p.row_bytes), kf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < NPR; ++r) acc = ffma2(qf[g][r], kf[r], acc);
+        a[g * kTPL + i] = acc.x + acc.y;
+      }
+    }
+#pragma unroll
+    for (int v = V; v < VP; ++v) a[v] = 0.f;
+    Butterfly<VP, LPR / 2>::run(a, lane);
+
+    // online softmax (base 2) for the lane's head
+    float sc[VF];
+    float mc = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < VF; ++u) {
+      const int t = (i_l0 + u) * RPI + rs;
+      sc[u] = t < n ? a[u] : -INFINITY;
+      mc = fmaxf(mc, sc[u]);
+    }
+#pragma unroll
+    for (int k = 0; k < IBITS; ++k) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 1 << (DUP + k)));
+#pragma unroll
+    for (int msk = LPR; msk < 32; msk <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, msk));
+    const float m_new = fmaxf(m_run, mc);
+    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = exp2f(m_run - m_use);
+    float psum = 0.f;
+#pragma unroll
+    for (int u = 0; u < VF; ++u) {
+      const float pv = exp2f(sc[u] - m_use);
+      psum += pv;
+      if (writer && g_l < G) p_tile[((i_l0 + u) * RPI + rs) * p.p_row + g_l] = pv;
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    if (head_leader) alpha_s[g_l] = alpha;
+    __syncwarp();
+
+    bool rescale = false;
+    float al[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      al[g] = alpha_s[g];
+      rescale |= al[g] != 1.f;
+    }
+    if (rescale) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int r = 0; r < NPR; ++r) o[g][r] = fmul2(o[g][r], make_float2(al[g], al[g]));
+    }
+
+    // o += p * V for this lane's 16 bytes of each row
+#pragma unroll
+    for (int i = 0; i < kTPL; ++i) {
+      const int t = i * RPI + rs;
+      if (t < n) {
+        float2 vf[NPR];
+        unpack16<T, NPR>(*reinterpret_cast<const uint4*>(vbuf + t * p.row_bytes), vf);
+        const float* prow = p_tile + t * p.p_row;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pg = prow[g];
+          const float2 pp = make_float2(pg, pg);
+#pragma unroll
+          for (int r = 0; r < NPR; ++r) o[g][r] = ffma2(pp, vf[r], o[g][r]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    if (flags & 2) {  // last chunk of the share: write the result
+#pragma unroll
+      for (int msk = LPR; msk < 32; msk <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int r = 0; r < NPR; ++r) {
+            o[g][r].x += __shfl_xor_sync(0xffffffffu, o[g][r].x, msk);
+            o[g][r].y += __shfl_xor_sync(0xffffffffu, o[g][r].y, msk);
+          }
+      float lt = l_run;
+#pragma unroll
+      for (int k = 0; k < IBITS; ++k) lt += __shfl_xor_sync(0xffffffffu, lt, 1 << (DUP + k));
+#pragma unroll
+      for (int msk = LPR; msk < 32; msk <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, msk);
+      if (head_leader) {
+        ml_s[2 * g_l] = m_run;
+        ml_s[2 * g_l + 1] = lt;
+      }
+      __syncwarp();
+      if (rs == 0) {
+        const bool whole = (flags & 4) != 0;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mg = ml_s[2 * g], lg = ml_s[2 * g + 1];
+          const float inv = lg > 0.f ? 1.f / lg : 0.f;
+          const int hq = h * G + g;
+          if (whole) {
+            char* dst = p.out + (static_cast<int64_t>(b) * p.Hq + hq) * Gm::RB + j * 16;
+            stg16(dst, pack16<T, NPR>(o[g], inv));
+          } else {
+            const int64_t slot = static_cast<int64_t>(c) + b;
+            float* dst = p.o_part + (slot * p.Hq + hq) * HD + j * Gm::DPL;
+#pragma unroll
+            for (int r = 0; r < NPR; r += 2)
+              *reinterpret_cast<float4*>(dst + 2 * r) =
+                  make_float4(o[g][r].x * inv, o[g][r].y * inv, o[g][r + 1].x * inv, o[g][r + 1].y * inv);
+            if (j == 0) p.lse_part[slot * p.Hq + hq] = lg > 0.f ? mg + log2f(lg) : -INFINITY;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// log-sum-exp merge of the partials of requests cut across CTAs
+// ---------------------------------------------------------------------------
+template <typename T, int HD>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const KParams p) {
+  const int b = blockIdx.x;
+  const int NC = p.cs[p.B];
+  const int cb0 = p.cs[b], cb1 = p.cs[b + 1];
+  if (cb1 <= cb0) return;
+  auto owner = [&](int x) {
+    return static_cast<int>(((static_cast<int64_t>(x) + 1) * p.n_ctas + NC - 1) / NC) - 1;
+  };
+  const int c0 = owner(cb0), c1 = owner(cb1 - 1);
+  if (c0 == c1) return;  // written whole by its CTA
+  constexpr int D4 = HD / 4;
+  for (int idx = threadIdx.x; idx < p.Hq * D4; idx += blockDim.x) {
+    const int hq = idx / D4, d4 = idx - hq * D4;
+    float M = -INFINITY;
+    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, p.lse_part[(static_cast<int64_t>(cc) + b) * p.Hq + hq]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+      for (int cc = c0; cc <= c1; ++cc) {
+        const int64_t slot = static_cast<int64_t>(cc) + b;
+        const float w = exp2f(p.lse_part[slot * p.Hq + hq] - M);
+        const float4 ov = *reinterpret_cast<const float4*>(p.o_part + (slot * p.Hq + hq) * HD + d4 * 4);
+        acc.x += w * ov.x;
+        acc.y += w * ov.y;
+        acc.z += w * ov.z;
+        acc.w += w * ov.w;
+        wsum += w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t e = (static_cast<int64_t>(b) * p.Hq + hq) * HD + d4 * 4;
+    if constexpr (sizeof(T) == 2) {
+      uint2 w;
+      w.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      w.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(p.out + e * 2) = w;
+    } else {
+      *reinterpret_cast<float4*>(p.out + e * 4) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+struct Fns {
+  const void* main = nullptr;
+  const void* merge = nullptr;
+};
+
+template <typename T, int HD>
+Fns fns_for_g(int G) {
+  switch (G) {
+    case 1: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 1>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 2: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 2>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 3: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 3>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 4: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 4>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 5: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 5>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 6: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 6>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 7: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 7>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    case 8: return {reinterpret_cast<const void*>(decode_kernel<T, HD, 8>), reinterpret_cast<const void*>(decode_merge_kernel<T, HD>)};
+    default: return {};
+  }
+}
+
+Fns get_fns(int dtype, int hd, int G) {
+  if (dtype == PA_BF16) return hd == 128 ? fns_for_g<__nv_bfloat16, 128>(G) : fns_for_g<__nv_bfloat16, 64>(G);
+  return hd == 128 ? fns_for_g<float, 128>(G) : fns_for_g<float, 64>(G);
+}
+
+// CTAs of one kernel instance that fit on an SM, cached per (device, kernel, smem).
+struct OccKey {
+  int device;
+  const void* fn;
+  int threads;
+  size_t smem;
+};
+std::mutex g_occ_mu;
+OccKey g_occ_keys[64];
+int g_occ_vals[64];
+int g_occ_n = 0;
+
+cudaError_t ctas_per_sm(const DeviceInfo& di, const void* fn, int threads, size_t smem, int* out) {
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    for (int i = 0; i < g_occ_n; ++i) {
+      const OccKey& k = g_occ_keys[i];
+      if (k.device == di.device && k.fn == fn && k.threads == threads && k.smem == smem) {
+        *out = g_occ_vals[i];
+        return cudaSuccess;
+      }
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  if (g_occ_n < 64) {
+    g_occ_keys[g_occ_n] = {di.device, fn, threads, smem};
+    g_occ_vals[g_occ_n] = n;
+    ++g_occ_n;
+  }
+  *out = n;
+  return cudaSuccess;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+cudaError_t plan_decode(const pa_cache_desc& d, int batch, int max_ctx, int max_ctas, DecodePlan* out) {
+  DeviceInfo di;
+  cudaError_t e = current_device_info(&di);
+  if (e != cudaSuccess) return e;
+  const int E = elem_bytes(d.dtype);
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const Fns f = get_fns(d.dtype, d.head_dim, G);
+  if (!f.main) return cudaErrorInvalidValue;
+  const int dpl = 16 / E, lpr = d.head_dim / dpl, rpi = 32 / lpr;
+  DecodePlan pl;
+  pl.nw = d.num_kv_heads;
+  pl.tokens_per_chunk = kTPL * rpi;
+  const int row_bytes = d.num_kv_heads * d.head_dim * E;
+  pl.chunk_bytes = pl.tokens_per_chunk * row_bytes;
+  pl.stages = kStages;
+  size_t off = static_cast<size_t>(kStages) * 2 * pl.chunk_bytes;
+  pl.off_bar = static_cast<uint32_t>(off);
+  off += 2 * kStages * sizeof(uint64_t);
+  pl.off_meta = static_cast<uint32_t>(align_up(off, 16));
+  off = pl.off_meta + kStages * 16;
+  pl.off_abort = static_cast<uint32_t>(off);
+  off += 16;
+  pl.p_row = G <= 4 ? 4 : 8;
+  pl.off_p = static_cast<uint32_t>(align_up(off, 16));
+  off = pl.off_p + static_cast<size_t>(pl.nw) * pl.tokens_per_chunk * pl.p_row * 4;
+  pl.off_alpha = static_cast<uint32_t>(off);
+  off += static_cast<size_t>(pl.nw) * 8 * 4;
+  pl.off_ml = static_cast<uint32_t>(off);
+  off += static_cast<size_t>(pl.nw) * 16 * 4;
+  pl.smem_bytes = align_up(off, 128);
+  if (pl.smem_bytes > static_cast<size_t>(di.max_smem_optin)) return cudaErrorInvalidValue;
+  int occ = 0;
+  e = ctas_per_sm(di, f.main, (pl.nw + 1) * 32, pl.smem_bytes, &occ);
+  if (e != cudaSuccess) return e;
+  const int64_t chunks_upper =
+      static_cast<int64_t>(batch) * ((max_ctx + pl.tokens_per_chunk - 1) / pl.tokens_per_chunk);
+  int64_t n = static_cast<int64_t>(occ) * di.sm_count;
+  if (max_ctas > 0) n = std::min<int64_t>(n, max_ctas);
+  n = std::min<int64_t>(n, std::max<int64_t>(1, chunks_upper));
+  pl.n_ctas = static_cast<int>(std::max<int64_t>(1, n));
+  size_t w = 0;
+  pl.ws_cs = w;
+  w = align_up(w + static_cast<size_t>(batch + 1) * 4, 256);
+  pl.ws_cta_seq = w;
+  w = align_up(w + static_cast<size_t>(pl.n_ctas) * 4, 256);
+  pl.ws_lse = w;
+  const size_t slots = static_cast<size_t>(pl.n_ctas) + batch;
+  w = align_up(w + slots * d.num_q_heads * 4, 256);
+  pl.ws_o = w;
+  w = align_up(w + slots * d.num_q_heads * d.head_dim * 4, 256);
+  pl.ws_bytes = w;
+  *out = pl;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const DecodeArgs& a, cudaStream_t s) {
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const Fns f = get_fns(d.dtype, d.head_dim, G);
+  if (!f.main) return cudaErrorInvalidValue;
+  char* ws = static_cast<char*>(a.workspace);
+  KParams p{};
+  p.q = static_cast<const char*>(a.q);
+  p.k_cache = static_cast<const char*>(a.k_cache);
+  p.v_cache = static_cast<const char*>(a.v_cache);
+  p.bt = a.block_tables;
+  p.ctx = a.context_lens;
+  p.out = static_cast<char*>(a.out);
+  p.o_part = reinterpret_cast<float*>(ws + pl.ws_o);
+  p.lse_part = reinterpret_cast<float*>(ws + pl.ws_lse);
+  p.cs = reinterpret_cast<int32_t*>(ws + pl.ws_cs);
+  p.cta_seq = reinterpret_cast<int32_t*>(ws + pl.ws_cta_seq);
+  p.err = a.err;
+  p.num_pages = d.num_pages;
+  p.B = a.batch;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.P = d.page_size;
+  p.maxp = a.max_pages;
+  p.max_ctx = a.max_context_len;
+  p.n_ctas = pl.n_ctas;
+  p.log2P = 0;
+  while ((1 << p.log2P) < d.page_size) ++p.log2P;
+  p.log2T = 0;
+  while ((1 << p.log2T) < pl.tokens_per_chunk) ++p.log2T;
+  p.row_bytes = d.num_kv_heads * d.head_dim * elem_bytes(d.dtype);
+  p.chunk_bytes = pl.chunk_bytes;
+  p.off_bar = pl.off_bar;
+  p.off_meta = pl.off_meta;
+  p.off_p = pl.off_p;
+  p.off_alpha = pl.off_alpha;
+  p.off_ml = pl.off_ml;
+  p.off_abort = pl.off_abort;
+  p.p_row = pl.p_row;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+
+  decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), args, pl.smem_bytes, s);
+  if (e != cudaSuccess) return e;
+  if (pl.n_ctas > 1) {
+    e = cudaLaunchKernel(f.merge, dim3(a.batch), dim3(kMergeThreads), args, 0, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,211 @@
+// Slot mapping, KV scatter, and the fused per-head Q/K RMSNorm + RoPE + KV
+// scatter (sm_103a).  All three are small, latency- or HBM-bound kernels.
+#include <math.h>
+
+#include <algorithm>
+
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+// ---------------------------------------------------------------------------
+// slot mapping (nano-vLLM learning note, prepare_prefill / prepare_decode)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) slot_mapping_kernel(const SlotMapParams p) {
+  const int b = blockIdx.x;
+  const int s0 = p.cu_seqlens_q[b], s1 = p.cu_seqlens_q[b + 1];
+  const int L = p.context_lens[b];
+  const int n = s1 - s0;
+  const int start = L - n;
+  const bool ok = n >= 0 && start >= 0 && s0 >= 0 && static_cast<int64_t>(s1) <= p.num_tokens &&
+                  static_cast<int64_t>(L) <= static_cast<int64_t>(p.max_pages) * p.page_size;
+  if (!ok) {
+    if (threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
+    // Leave well-formed rows of this request marked "store nothing".
+    if (n > 0 && s0 >= 0 && static_cast<int64_t>(s1) <= p.num_tokens)
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        p.positions[s0 + j] = 0;
+        p.slots[s0 + j] = -1;
+      }
+    return;
+  }
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int pos = start + j;
+    const int page = p.block_tables[static_cast<int64_t>(b) * p.max_pages + pos / p.page_size];
+    int64_t slot = -1;
+    if (page >= 0 && page < p.num_pages) {
+      slot = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+    } else {
+      raise_flag(p.err, PA_DEVERR_BAD_PAGE);
+    }
+    p.positions[s0 + j] = pos;
+    p.slots[s0 + j] = slot;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// KV scatter (nano-vLLM learning note, store_kvcache_kernel): 16-byte chunks,
+// one thread per chunk of K and the same chunk of V.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
+  const uint32_t cpr = static_cast<uint32_t>(p.row_bytes) >> 4;
+  const int64_t total = p.n_tokens * cpr;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / cpr;
+    const uint32_t ch = static_cast<uint32_t>(i - t * cpr);
+    const int64_t slot = p.slots[t];
+    if (slot < 0 || slot >= p.num_slots) {
+      if (slot != -1 && ch == 0) raise_flag(p.err, PA_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const uint4 kw = ldg16(p.k + t * p.k_stride_bytes + ch * 16);
+    const uint4 vw = ldg16(p.v + t * p.v_stride_bytes + ch * 16);
+    stg16(p.k_cache + slot * p.row_bytes + ch * 16, kw);
+    stg16(p.v_cache + slot * p.row_bytes + ch * 16, vw);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fused q/k RMSNorm + rotary + KV scatter.  One CTA (4 warps) per token.
+// A group of LPH lanes handles one head: lane l owns elements
+// [4l, 4l+4) of the first half and the same of the second half, so each lane
+// holds both members of its rotation pairs.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Vec4;
+template <>
+struct Vec4<float> {
+  static PA_DEVINL void load(const void* p, float (&x)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+  static PA_DEVINL void store(void* p, const float (&x)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  }
+};
+template <>
+struct Vec4<__nv_bfloat16> {
+  static PA_DEVINL void load(const void* p, float (&x)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const float2 a = bf16x2_to_float2(v.x), b = bf16x2_to_float2(v.y);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  }
+  static PA_DEVINL void store(void* p, const float (&x)[4]) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+  }
+};
+
+// 2*pi split into a double and the double nearest to the remainder.
+constexpr double kTwoPiHi = 6.283185307179586;
+constexpr double kTwoPiLo = 2.4492935982947064e-16;
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(128) norm_rope_kv_write_kernel(const NormRopeParams p) {
+  constexpr int E = sizeof(T);
+  constexpr int PE = 4;
+  constexpr int LPH = HD / (2 * PE);  // lanes per head
+  constexpr int HPW = 32 / LPH;       // heads per warp pass
+  const int64_t t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPH, l = lane % LPH;
+  const int pos = p.positions[t];
+  const int64_t slot = p.slots[t];
+  const bool slot_ok = slot >= 0 && slot < p.num_slots;
+  if (!slot_ok && slot != -1 && threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_SLOT);
+
+  // cos / sin of this lane's pair indices: the angle pos * theta^(-2i/HD) is
+  // formed and reduced modulo 2*pi in double, then evaluated in float.
+  float cs[PE], sn[PE];
+#pragma unroll
+  for (int e = 0; e < PE; ++e) {
+    const double ang = static_cast<double>(pos) * p.inv_freq[l * PE + e];
+    const double k = rint(ang * (1.0 / kTwoPiHi));
+    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
+    sincosf(static_cast<float>(r), &sn[e], &cs[e]);
+  }
+  float wq_a[PE], wq_b[PE], wk_a[PE], wk_b[PE];
+  Vec4<T>::load(static_cast<const T*>(p.wq) + l * PE, wq_a);
+  Vec4<T>::load(static_cast<const T*>(p.wq) + HD / 2 + l * PE, wq_b);
+  Vec4<T>::load(static_cast<const T*>(p.wk) + l * PE, wk_a);
+  Vec4<T>::load(static_cast<const T*>(p.wk) + HD / 2 + l * PE, wk_b);
+
+  const int nheads = p.hq + p.hkv;
+  for (int hh = warp * HPW + sub; hh - sub < nheads; hh += 4 * HPW) {
+    const bool active = hh < nheads;
+    const bool isq = hh < p.hq;
+    const T* src = isq ? static_cast<const T*>(p.q) + t * p.q_stride + static_cast<int64_t>(hh) * HD
+                       : static_cast<const T*>(p.k) + t * p.k_stride + static_cast<int64_t>(hh - p.hq) * HD;
+    float xa[PE] = {0.f, 0.f, 0.f, 0.f}, xb[PE] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      Vec4<T>::load(src + l * PE, xa);
+      Vec4<T>::load(src + HD / 2 + l * PE, xb);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < PE; ++e) ss += xa[e] * xa[e] + xb[e] * xb[e];
+#pragma unroll
+    for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    if (!active) continue;
+    const float r = 1.0f / sqrtf(ss / HD + p.eps);
+    float ya[PE], yb[PE];
+#pragma unroll
+    for (int e = 0; e < PE; ++e) {
+      const float na = round_to<T>(round_to<T>(xa[e] * r) * (isq ? wq_a[e] : wk_a[e]));
+      const float nb = round_to<T>(round_to<T>(xb[e] * r) * (isq ? wq_b[e] : wk_b[e]));
+      ya[e] = round_to<T>(na * cs[e] - nb * sn[e]);
+      yb[e] = round_to<T>(nb * cs[e] + na * sn[e]);
+    }
+    if (isq) {
+      T* dst = static_cast<T*>(p.q_out) + (t * p.hq + hh) * HD;
+      Vec4<T>::store(dst + l * PE, ya);
+      Vec4<T>::store(dst + HD / 2 + l * PE, yb);
+    } else if (slot_ok) {
+      T* dst = static_cast<T*>(p.k_cache) + (slot * p.hkv + (hh - p.hq)) * HD;
+      Vec4<T>::store(dst + l * PE, ya);
+      Vec4<T>::store(dst + HD / 2 + l * PE, yb);
+    }
+  }
+  if (slot_ok) {
+    const int row_bytes = p.hkv * HD * E;
+    const char* vsrc = static_cast<const char*>(p.v) + t * p.v_stride * E;
+    char* vdst = static_cast<char*>(p.v_cache) + slot * row_bytes;
+    for (int ch = threadIdx.x; ch < row_bytes / 16; ch += blockDim.x)
+      stg16(vdst + ch * 16, ldg16(vsrc + ch * 16));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(const SlotMapParams& p, cudaStream_t s) {
+  if (p.batch == 0) return cudaSuccess;
+  slot_mapping_kernel<<<p.batch, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t s) {
+  if (p.n_tokens == 0) return cudaSuccess;
+  DeviceInfo di;
+  cudaError_t e = current_device_info(&di);
+  if (e != cudaSuccess) return e;
+  const int64_t total = p.n_tokens * (p.row_bytes / 16);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(di.sm_count) * 8);
+  kv_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_rope_kv_write(int dtype, int head_dim, const NormRopeParams& p, cudaStream_t s) {
+  if (p.n_tokens == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(p.n_tokens);
+  if (dtype == PA_BF16) {
+    if (head_dim == 128) norm_rope_kv_write_kernel<__nv_bfloat16, 128><<<grid, 128, 0, s>>>(p);
+    else norm_rope_kv_write_kernel<__nv_bfloat16, 64><<<grid, 128, 0, s>>>(p);
+  } else {
+    if (head_dim == 128) norm_rope_kv_write_kernel<float, 128><<<grid, 128, 0, s>>>(p);
+    else norm_rope_kv_write_kernel<float, 64><<<grid, 128, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

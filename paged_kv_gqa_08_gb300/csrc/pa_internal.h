@@ -1,0 +1,149 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units.  Host-side C++ only; nothing here is exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Cached properties of one device.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_optin = 0;  // bytes per block with the opt-in attribute
+  int cc_major = 0, cc_minor = 0;
+};
+// Properties of the current device (queried once per device).
+cudaError_t current_device_info(DeviceInfo* out);
+
+// Address of the device error word on the current device.
+cudaError_t device_error_word(unsigned int** out);
+
+inline int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+// ---------------------------------------------------------------------------
+// slot mapping / KV write / fused norm + rope + KV write
+// ---------------------------------------------------------------------------
+struct SlotMapParams {
+  const int32_t* cu_seqlens_q;
+  const int32_t* context_lens;
+  const int32_t* block_tables;
+  int32_t* positions;
+  int64_t* slots;
+  unsigned int* err;
+  int64_t num_pages;
+  int64_t num_tokens;
+  int32_t batch, page_size, max_pages;
+};
+cudaError_t launch_slot_mapping(const SlotMapParams& p, cudaStream_t s);
+
+struct KvWriteParams {
+  const char* k;
+  const char* v;
+  int64_t k_stride_bytes, v_stride_bytes;
+  int64_t n_tokens;
+  const int64_t* slots;
+  char* k_cache;
+  char* v_cache;
+  int64_t num_slots;
+  int32_t row_bytes;
+  unsigned int* err;
+};
+cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t s);
+
+struct NormRopeParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t q_stride, k_stride, v_stride;  // elements
+  int64_t n_tokens;
+  const int32_t* positions;
+  const void* wq;
+  const void* wk;
+  const int64_t* slots;
+  void* q_out;
+  void* k_cache;
+  void* v_cache;
+  int64_t num_slots;
+  unsigned int* err;
+  float eps;
+  int32_t hq, hkv;
+  double inv_freq[64];  // theta^(-2i/head_dim), computed on the host in double
+};
+cudaError_t launch_norm_rope_kv_write(int dtype, int head_dim, const NormRopeParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+struct DecodePlan {
+  int nw = 0;            // consumer warps per CTA (= num_kv_heads)
+  int tokens_per_chunk = 0;
+  int chunk_bytes = 0;   // K (or V) bytes of one chunk in shared memory
+  int stages = 0;
+  int n_ctas = 0;        // partitions of the key space
+  size_t smem_bytes = 0;
+  // workspace layout (byte offsets)
+  size_t ws_cs = 0, ws_cta_seq = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
+  // shared-memory layout (byte offsets)
+  uint32_t off_bar = 0, off_meta = 0, off_p = 0, off_alpha = 0, off_ml = 0, off_abort = 0;
+  int p_row = 0;         // floats per token row of the probability tile
+};
+// Plan for the current device; returns cudaErrorInvalidValue for an
+// unsupported shape.
+cudaError_t plan_decode(const pa_cache_desc& d, int batch, int max_context_len, int max_ctas,
+                        DecodePlan* out);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  void* workspace;
+  unsigned int* err;
+  int32_t batch, max_pages, max_context_len;
+  float scale;
+};
+cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& plan, const DecodeArgs& a,
+                          cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// prefill
+// ---------------------------------------------------------------------------
+struct PrefillArgs {
+  const void* q;
+  const int32_t* cu_seqlens_q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  unsigned int* err;
+  int64_t num_tokens;
+  int32_t batch, max_seqlen_q, max_pages, max_context_len;
+  float scale;
+};
+// CUDA-core kernel (any supported dtype / head_dim).
+cudaError_t launch_prefill_simt(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s);
+// tcgen05 tensor-core kernel (bf16, head_dim 128).
+cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// metadata validation
+// ---------------------------------------------------------------------------
+struct ValidateArgs {
+  const int32_t* cu_seqlens_q;
+  const int32_t* context_lens;
+  const int32_t* block_tables;
+  int32_t* error_count;
+  int64_t num_pages;
+  int32_t batch, max_pages, max_context_len, page_size;
+};
+cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
+
+}  // namespace pa

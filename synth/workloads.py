@@ -26,8 +26,10 @@ softmax.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -37,9 +39,13 @@ BF16_NAN_BITS = np.uint16(0x7FC0)
 
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (nearest, ties to even); return the bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    bias = u >> np.uint32(16)
+    bias &= np.uint32(1)
+    bias += np.uint32(0x7FFF)
+    u += bias
+    u >>= np.uint32(16)
+    return u.astype(np.uint16)
 
 
 def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:
@@ -47,15 +53,28 @@ def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal_storage(rng: np.random.Generator, shape, dtype: str, block: int = 1 << 24) -> np.ndarray:
-    """Draw N(0,1) values of `shape` and store them in the config dtype."""
+def _normal_storage(rng: np.random.Generator, shape, dtype: str, block: int = 1 << 22) -> np.ndarray:
+    """Draw N(0,1) values of `shape` and store them in the config dtype.
+
+    The array is cut into blocks of `block` values; one draw from `rng` gives
+    each block its own seed, and the blocks are filled in parallel.  The values
+    depend only on `rng`'s state, never on the thread count.
+    """
     n = int(np.prod(shape))
-    if dtype == "f32":
-        return rng.standard_normal(n, dtype=np.float32).reshape(shape)
-    out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, block):
-        e = min(n, s + block)
-        out[s:e] = bf16_bits_from_f32(rng.standard_normal(e - s, dtype=np.float32))
+    nb = max(1, -(-n // block))
+    seeds = rng.integers(0, np.iinfo(np.int64).max, size=nb, dtype=np.int64)
+    out = np.empty(n, dtype=np.float32 if dtype == "f32" else np.uint16)
+
+    def fill(i: int) -> None:
+        s, e = i * block, min(n, (i + 1) * block)
+        x = np.random.default_rng(int(seeds[i])).standard_normal(e - s, dtype=np.float32)
+        out[s:e] = x if dtype == "f32" else bf16_bits_from_f32(x)
+
+    if nb == 1:
+        fill(0)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=min(nb, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(nb)))
     return out.reshape(shape)
 
 
@@ -248,3 +267,24 @@ def make_workload(name_or_spec, seed: Optional[int] = None, **overrides) -> Work
         block_tables=bt, hist_k=hist_k, hist_v=hist_v, k_new=k_new, v_new=v_new,
         q=q, q_norm_w=q_w, k_norm_w=k_w, eps=eps, rope_theta=theta,
         scale=float(spec.get("scale", 1.0 / math.sqrt(hd))), seed=int(seed))
+
+
+def to_torch(wl: Workload, device="cuda") -> dict:
+    """The workload's arrays as torch tensors on `device` (bit-identical values).
+
+    bf16 arrays travel as their uint16 bit patterns and are reinterpreted, so
+    no value is rounded again on the way.
+    """
+    import torch
+
+    def arr(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    out = {k: arr(getattr(wl, k)) for k in ("hist_k", "hist_v", "k_new", "v_new", "q", "q_norm_w", "k_norm_w",
+                                             "context_lens", "new_lens", "cu_seqlens_q", "hist_lens", "cu_hist",
+                                             "block_tables")}
+    return out

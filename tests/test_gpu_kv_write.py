@@ -1,0 +1,97 @@
+"""GPU parity of the slot mapping and the KV write (bit-exact), and of the
+fused q/k RMSNorm + RoPE (within two bf16 units in the last place)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_harness import GpuRun, storage
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
+
+
+def _ordered(bits: np.ndarray, width: int) -> np.ndarray:
+    """Map float bit patterns to integers that are monotone in the value."""
+    b = bits.astype(np.int64)
+    sign = 1 << (width - 1)
+    return np.where(b & sign, sign - (b & (sign - 1)), sign + b)
+
+
+def _max_ulps(a: np.ndarray, b: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return int(np.max(np.abs(_ordered(a, 16) - _ordered(b, 16)))) if a.size else 0
+    return int(np.max(np.abs(_ordered(a.view(np.uint32), 32) - _ordered(b.view(np.uint32), 32)))) if a.size else 0
+
+
+def _bits(a: np.ndarray) -> np.ndarray:
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+@pytest.mark.parametrize("name", synth.CONFIG_ORDER + ["prefill_2k"])
+def test_step_slot_mapping_and_cache_write(name):
+    wl = synth.make_workload(name)
+    run = GpuRun(wl)
+    run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl, with_attention=False)
+    n = wl.num_new_tokens
+    # slot mapping: exact
+    assert np.array_equal(run.bufs.positions[:n].cpu().numpy(), ref["positions"])
+    assert np.array_equal(run.bufs.slots[:n].cpu().numpy(), ref["slots"])
+    _, hist_slots = oracle.slot_mapping(wl.block_tables, wl.hist_lens, wl.cu_hist, wl.page_size)
+    assert np.array_equal(run.hist_slots[: len(hist_slots)].cpu().numpy(), hist_slots)
+    kc, vc = storage(run.k_cache), storage(run.v_cache)
+    # V is a pure copy everywhere; poison (NaN) bits of never-written slots match too
+    assert np.array_equal(_bits(vc), _bits(ref["v_cache"]))
+    if wl.q_norm_w is None:
+        assert np.array_equal(_bits(kc), _bits(ref["k_cache"]))
+        return
+    # k of the new tokens went through RMSNorm + RoPE: compare those rows within
+    # 2 bf16 ulps, everything else bit for bit
+    flat_g = kc.reshape(-1, wl.num_kv_heads * wl.head_dim)
+    flat_r = ref["k_cache"].reshape(-1, wl.num_kv_heads * wl.head_dim)
+    new = ref["slots"]
+    mask = np.ones(flat_g.shape[0], bool)
+    mask[new] = False
+    assert np.array_equal(flat_g[mask], flat_r[mask])
+    assert _max_ulps(flat_g[new], flat_r[new]) <= 2
+    assert _max_ulps(storage(run.bufs.q_out[:n]), ref["q"]) <= 2
+
+
+def test_kv_write_skips_minus_one_and_flags_bad_slots():
+    from paged_kv_gqa_08_gb300 import (PA_DEVERR_BAD_SLOT, cache_desc, PA_BF16, pa_kv_write,
+                                       pa_read_device_errors)
+    pa_read_device_errors(reset=True)
+    dev = "cuda"
+    desc = cache_desc(4, 2, 64, 16, 4, PA_BF16)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    k = torch.randn(5, 2, 64, device=dev).to(torch.bfloat16)
+    v = torch.randn(5, 2, 64, device=dev).to(torch.bfloat16)
+    slots = torch.tensor([3, -1, 63, 64, 0], dtype=torch.int64, device=dev)   # 64 is out of range
+    pa_kv_write(desc, k, 128, v, 128, 5, slots, kc, vc)
+    torch.cuda.synchronize()
+    fk = kc.view(64, 128)
+    assert torch.equal(fk[3], k[0].view(-1)) and torch.equal(fk[63], k[2].view(-1)) and torch.equal(fk[0], k[4].view(-1))
+    untouched = [s for s in range(64) if s not in (0, 3, 63)]
+    assert torch.count_nonzero(fk[untouched]) == 0
+    assert pa_read_device_errors(reset=True) & PA_DEVERR_BAD_SLOT
+
+
+def test_kv_write_from_fused_qkv_rows():
+    # k and v as strided views into one [N, (Hq + 2 Hkv) * hd] projection output
+    from paged_kv_gqa_08_gb300 import cache_desc, PA_BF16, pa_kv_write
+    dev = "cuda"
+    Hq, Hkv, hd, N = 16, 8, 128, 37
+    qkv = torch.randn(N, (Hq + 2 * Hkv) * hd, device=dev).to(torch.bfloat16)
+    k = qkv[:, Hq * hd:(Hq + Hkv) * hd]
+    v = qkv[:, (Hq + Hkv) * hd:]
+    desc = cache_desc(Hq, Hkv, hd, 16, 8, PA_BF16)
+    kc = torch.zeros(8, 16, Hkv, hd, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    slots = torch.randperm(128, device=dev)[:N].to(torch.int64)
+    pa_kv_write(desc, k, qkv.stride(0), v, qkv.stride(0), N, slots, kc, vc)
+    torch.cuda.synchronize()
+    assert torch.equal(kc.view(128, -1)[slots], k)
+    assert torch.equal(vc.view(128, -1)[slots], v)

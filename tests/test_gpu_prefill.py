@@ -1,0 +1,85 @@
+"""GPU parity of chunked prefill (norm + rope + KV write + attention) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_harness import GpuRun, as_f64
+from paged_kv_gqa_08_gb300 import pa_decode, pa_prefill_varlen, pa_read_device_errors
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
+
+
+def _check(out, ref, dtype):
+    ok, err, bound = oracle.within_tolerance(as_f64(out), ref, dtype)
+    assert ok, f"max abs err {err:.3e} > bound {bound:.3e}"
+    return err
+
+
+@pytest.mark.parametrize("name", ["qwen3_0p6b_chunked_prefill", "prefill_2k"])
+def test_prefill_configs_match_oracle(name):
+    wl = synth.make_workload(name)
+    pa_read_device_errors(reset=True)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
+
+
+SMALL = [
+    # dtype, Hq, Hkv, hd, P, chunks, prefixes, norm
+    ("bf16", 16, 8, 128, 16, [1, 7, 63, 64, 65, 129, 300], [0, 5, 127, 128, 200, 1000, 33], True),
+    ("bf16", 16, 8, 128, 256, [130, 1, 64], [0, 257, 700], False),
+    ("bf16", 8, 8, 128, 16, [200, 3], [50, 0], True),           # G = 1
+    ("bf16", 16, 4, 128, 32, [37, 90], [11, 300], True),        # G = 4
+    ("bf16", 32, 4, 128, 16, [17, 40], [160, 2], False),        # G = 8
+    ("bf16", 24, 8, 128, 16, [45, 12], [9, 130], True),         # G = 3
+    ("bf16", 20, 4, 128, 64, [30, 26], [64, 1], False),         # G = 5
+    ("bf16", 8, 4, 64, 16, [20, 5], [40, 0], True),             # head_dim 64 (CUDA-core kernel)
+    ("f32", 4, 2, 64, 16, [1, 9, 33], [0, 16, 5], True),
+    ("f32", 8, 4, 128, 32, [70, 2], [0, 100], False),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"{c[0]}-hq{c[1]}-hkv{c[2]}-d{c[3]}-p{c[4]}-{'norm' if c[7] else 'plain'}"
+                                             for c in SMALL])
+def test_prefill_small_shapes(case):
+    dtype, Hq, Hkv, hd, P, chunks, prefixes, norm = case
+    spec = dict(kind="prefill", dtype=dtype, B=len(chunks), Hq=Hq, Hkv=Hkv, hd=hd, P=P, chunks=chunks,
+                prefixes=prefixes, norm=norm, seed=sum(chunks) + 7)
+    wl = synth.make_workload(spec)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
+
+
+def test_prefill_with_length_one_chunks_matches_decode():
+    wl = synth.make_workload("qwen3_0p6b_decode", B=16)
+    run = GpuRun(wl)
+    out_dec = run.step().clone()
+    out_pf = torch.empty_like(out_dec)
+    pa_prefill_varlen(run.desc, run.t["q"], run.t["cu_seqlens_q"], wl.batch, 1, wl.batch, run.k_cache, run.v_cache,
+                      run.t["block_tables"], wl.max_pages_per_seq, run.t["context_lens"], wl.max_context_len,
+                      wl.scale, out_pf)
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out_dec[: wl.batch], ref["o"], wl.dtype)
+    _check(out_pf[: wl.batch], ref["o"], wl.dtype)
+
+
+def test_prefill_empty_requests_in_batch():
+    # requests with no new tokens are skipped; the others are unaffected
+    spec = dict(kind="prefill", dtype="bf16", B=4, Hq=16, Hkv=8, hd=128, P=16, chunks=[0, 40, 0, 3],
+                prefixes=[10, 20, 0, 64], norm=True, seed=99)
+    wl = synth.make_workload(spec)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
