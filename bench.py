@@ -265,11 +265,18 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (the timing rule: the slowest rank)."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, elapsed_ms_max: float, world: int) -> float:
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (elapsed_ms_max * 1e-3)
 
 
 def time_device_steps(d: Device, steps: int, warmup: int, world: int, clocks: ClockSampler = None):
@@ -458,8 +465,8 @@ def main():
     total_ms, attn_ms, write_ms = time_device_steps(d, args.steps, args.warmup, world, clocks)
     ms = total_ms / args.steps
     step_bytes = decode_call_bytes(wl) + write_bytes(wl)
-    value = world * step_bytes / (ms * 1e-3) / 1e9
-    tok_s = world * wl.batch / (ms * 1e-3)
+    value = whole_job_rate(step_bytes, ms, world) / 1e9
+    tok_s = whole_job_rate(wl.batch, ms, world)
     dec_bytes = decode_call_bytes(wl)
     achieved = dec_bytes / (attn_ms * 1e-3) / 1e9
     traffic = profiled_traffic("decode_qwen3_0p6b", ["decode.cu", "pa_common.cuh"])

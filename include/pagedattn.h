@@ -237,6 +237,16 @@ PA_API pa_status pa_validate_metadata(const pa_cache_desc* desc, int32_t batch,
                                int32_t max_context_len, int32_t* error_count, pa_stream_t stream);
 
 /*
+ * pa_selftest_bounded_wait -- exercises the kernels' bounded-wait path.  Launches
+ * one thread that waits on an mbarrier nothing ever arrives on; after
+ * timeout_ms (1 .. 10000) the wait gives up, the kernel raises
+ * PA_DEVERR_TIMEOUT and exits, and the context stays usable.  Every wait in
+ * the other kernels ends the same way (with a 2 s limit), so a lost copy or
+ * MMA completion costs a flagged, wrong result instead of a hung GPU.
+ */
+PA_API pa_status pa_selftest_bounded_wait(int32_t timeout_ms, pa_stream_t stream);
+
+/*
  * pa_read_device_errors -- the PA_DEVERR_* flags raised on the current device
  * since the last reset (host out).  Synchronises the device.  reset != 0
  * clears the flags.

@@ -82,6 +82,7 @@ _SIGS = {
                          _VP]),
     "pa_prefill_varlen": (_I32, [_DESC, _VP, _VP, _I32, _I32, _I64, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _VP, _VP]),
     "pa_validate_metadata": (_I32, [_DESC, _I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP]),
+    "pa_selftest_bounded_wait": (_I32, [_I32, _VP]),
     "pa_read_device_errors": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32]),
     "pa_last_cuda_error": (_I32, []),
     "pa_status_string": (ctypes.c_char_p, [_I32]),
@@ -196,6 +197,10 @@ def pa_validate_metadata(desc, batch, cu_seqlens_q, context_lens, block_tables, 
     _check("pa_validate_metadata", lib.pa_validate_metadata(
         ctypes.byref(desc), batch, _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables), max_pages_per_seq,
         max_context_len, _ptr(error_count), _stream(stream)))
+
+
+def pa_selftest_bounded_wait(timeout_ms: int, stream=None):
+    _check("pa_selftest_bounded_wait", load_library().pa_selftest_bounded_wait(timeout_ms, _stream(stream)))
 
 
 def pa_read_device_errors(reset: bool = False) -> int:

@@ -51,7 +51,12 @@ bool stride_ok(const pa_cache_desc* d, int64_t stride, int64_t min_elems) {
   return stride >= min_elems && (stride * elem_bytes(d->dtype)) % 16 == 0;
 }
 
+// Called by every entry point once its arguments are validated, before it
+// launches anything: fetches the device error word and clears a launch error
+// left pending by earlier, unrelated CUDA calls, so that the error checked
+// after our own launches is ours.
 pa_status prepare(unsigned int** err) {
+  (void)cudaGetLastError();
   cudaError_t e = device_error_word(err);
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -332,6 +337,15 @@ pa_status pa_validate_metadata(const pa_cache_desc* desc, int32_t batch, const i
   a.max_context_len = max_context_len;
   a.page_size = desc->page_size;
   cudaError_t e = launch_validate(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_selftest_bounded_wait(int32_t timeout_ms, pa_stream_t stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return PA_ERR_SHAPE;
+  unsigned int* err = nullptr;
+  pa_status st = prepare(&err);
+  if (st != PA_OK) return st;
+  cudaError_t e = launch_bounded_wait_selftest(err, timeout_ms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

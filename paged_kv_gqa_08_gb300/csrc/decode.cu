@@ -486,15 +486,22 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const KPara
   };
   const int c0 = owner(cb0), c1 = owner(cb1 - 1);
   if (c0 == c1) return;  // written whole by its CTA
+  // With more CTAs than chunks some CTAs between c0 and c1 own no chunk and
+  // wrote no partial: only CTAs with a non-empty range take part.
+  auto busy = [&](int c) {
+    return (static_cast<int64_t>(c) * NC) / p.n_ctas < (static_cast<int64_t>(c + 1) * NC) / p.n_ctas;
+  };
   constexpr int D4 = HD / 4;
   for (int idx = threadIdx.x; idx < p.Hq * D4; idx += blockDim.x) {
     const int hq = idx / D4, d4 = idx - hq * D4;
     float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, p.lse_part[(static_cast<int64_t>(cc) + b) * p.Hq + hq]);
+    for (int cc = c0; cc <= c1; ++cc)
+      if (busy(cc)) M = fmaxf(M, p.lse_part[(static_cast<int64_t>(cc) + b) * p.Hq + hq]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (M != -INFINITY) {
       for (int cc = c0; cc <= c1; ++cc) {
+        if (!busy(cc)) continue;
         const int64_t slot = static_cast<int64_t>(cc) + b;
         const float w = exp2f(p.lse_part[slot * p.Hq + hq] - M);
         const float4 ov = *reinterpret_cast<const float4*>(p.o_part + (slot * p.Hq + hq) * HD + d4 * 4);
@@ -569,7 +576,10 @@ cudaError_t ctas_per_sm(const DeviceInfo& di, const void* fn, int threads, size_
       }
     }
   }
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // The attribute is per kernel, not per launch: raise it to the device's
+  // opt-in maximum so every plan's shared-memory size fits.
+  cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
   if (e != cudaSuccess) return e;
   int n = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);

@@ -76,17 +76,18 @@ PA_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // sets the CTA's abort flag and returns false, so a kernel can never hang.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-// Wait for phase `parity` of `bar`.  Returns false on timeout or when another
-// thread of the CTA has already aborted (`*abort` != 0).
+// Wait for phase `parity` of `bar`.  Returns false on timeout (after
+// `limit_ns`) or when another thread of the CTA has already aborted
+// (`*abort` != 0).
 PA_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                 unsigned int* err) {
+                                 unsigned int* err, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         raise_flag(err, PA_DEVERR_TIMEOUT);
         return false;

@@ -145,5 +145,6 @@ struct ValidateArgs {
   int32_t batch, max_pages, max_context_len, page_size;
 };
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s);
+cudaError_t launch_bounded_wait_selftest(unsigned int* err, int timeout_ms, cudaStream_t s);
 
 }  // namespace pa

@@ -29,7 +29,24 @@ __global__ void __launch_bounds__(128) validate_kernel(const ValidateArgs a) {
   if (bad) atomicAdd(a.error_count, bad);
 }
 
+// One thread waits for an mbarrier phase that never completes; the bounded
+// wait gives up after limit_ns and raises PA_DEVERR_TIMEOUT.
+__global__ void bounded_wait_selftest_kernel(unsigned int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait_bounded(&bar, 0, &abort_flag, err, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(unsigned int* err, int timeout_ms, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(err, static_cast<uint64_t>(timeout_ms) * 1000000ull);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_validate(const ValidateArgs& a, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(a.error_count, 0, sizeof(int32_t), s);

@@ -11,17 +11,19 @@ from gpu_harness import GpuRun, storage
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
 
-def _ordered(bits: np.ndarray, width: int) -> np.ndarray:
-    """Map float bit patterns to integers that are monotone in the value."""
-    b = bits.astype(np.int64)
-    sign = 1 << (width - 1)
-    return np.where(b & sign, sign - (b & (sign - 1)), sign + b)
-
-
-def _max_ulps(a: np.ndarray, b: np.ndarray) -> int:
-    if a.dtype == np.uint16:
-        return int(np.max(np.abs(_ordered(a, 16) - _ordered(b, 16)))) if a.size else 0
-    return int(np.max(np.abs(_ordered(a.view(np.uint32), 32) - _ordered(b.view(np.uint32), 32)))) if a.size else 0
+def _close_on_unit_scale(got: np.ndarray, ref: np.ndarray, dtype: str) -> None:
+    """Normed + rotated values: |got - ref| <= 2 units in the last place of
+    max(|ref|, 1) for bf16 (16 for fp32, whose unit is far below the fp32
+    evaluation error of rsqrt, sincos and the rotation).  Normalised rows have elements of order one; three roundings
+    to the storage dtype happen on the way (after x*r, after *w, after the
+    rotation) and the rotation mixes two rounded values, so where its result
+    cancels towards zero the error is on the scale of its inputs, not of the
+    result."""
+    g, r = oracle.widen(got, dtype), oracle.widen(ref, dtype)
+    units = 2 * 2.0 ** -7 if dtype == "bf16" else 16 * 2.0 ** -23
+    tol = units * np.maximum(np.abs(r), 1.0)
+    bad = np.abs(g - r) > tol
+    assert not np.any(bad), f"{int(bad.sum())} values off by up to {float(np.max(np.abs(g - r))):.3e}"
 
 
 def _bits(a: np.ndarray) -> np.ndarray:
@@ -47,16 +49,16 @@ def test_step_slot_mapping_and_cache_write(name):
     if wl.q_norm_w is None:
         assert np.array_equal(_bits(kc), _bits(ref["k_cache"]))
         return
-    # k of the new tokens went through RMSNorm + RoPE: compare those rows within
-    # 2 bf16 ulps, everything else bit for bit
+    # k of the new tokens went through RMSNorm + RoPE: compare those rows on
+    # the scale of the normalised values, everything else bit for bit
     flat_g = kc.reshape(-1, wl.num_kv_heads * wl.head_dim)
     flat_r = ref["k_cache"].reshape(-1, wl.num_kv_heads * wl.head_dim)
     new = ref["slots"]
     mask = np.ones(flat_g.shape[0], bool)
     mask[new] = False
     assert np.array_equal(flat_g[mask], flat_r[mask])
-    assert _max_ulps(flat_g[new], flat_r[new]) <= 2
-    assert _max_ulps(storage(run.bufs.q_out[:n]), ref["q"]) <= 2
+    _close_on_unit_scale(flat_g[new], flat_r[new], wl.dtype)
+    _close_on_unit_scale(storage(run.bufs.q_out[:n]), ref["q"], wl.dtype)
 
 
 def test_kv_write_skips_minus_one_and_flags_bad_slots():
