@@ -13,15 +13,17 @@ pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
 def _close_on_unit_scale(got: np.ndarray, ref: np.ndarray, dtype: str) -> None:
     """Normed + rotated values: |got - ref| <= 2 units in the last place of
-    max(|ref|, 1) for bf16 (16 for fp32, whose unit is far below the fp32
+    max(|got|, |ref|, 1) for bf16 (16 for fp32, whose unit is far below the fp32
     evaluation error of rsqrt, sincos and the rotation).  Normalised rows have elements of order one; three roundings
     to the storage dtype happen on the way (after x*r, after *w, after the
     rotation) and the rotation mixes two rounded values, so where its result
     cancels towards zero the error is on the scale of its inputs, not of the
     result."""
     g, r = oracle.widen(got, dtype), oracle.widen(ref, dtype)
-    units = 2 * 2.0 ** -7 if dtype == "bf16" else 16 * 2.0 ** -23
-    tol = units * np.maximum(np.abs(r), 1.0)
+    mant, units = (7, 2) if dtype == "bf16" else (23, 16)
+    scale = np.maximum(np.maximum(np.abs(g), np.abs(r)), 1.0)
+    ulp = np.exp2(np.floor(np.log2(scale)) - mant)      # unit in the last place at that scale
+    tol = units * ulp
     bad = np.abs(g - r) > tol
     assert not np.any(bad), f"{int(bad.sum())} values off by up to {float(np.max(np.abs(g - r))):.3e}"
 
