@@ -197,6 +197,31 @@ PA_API pa_status pa_decode(const pa_cache_desc* desc, const void* q, int32_t bat
                     pa_stream_t stream);
 
 /*
+ * pa_decode_no_alloc -- pa_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this call.
+ *
+ * For code that cannot call cudaMalloc where it runs decode (a plugin handed
+ * only its buffers, a framework that forbids allocations while it builds a CUDA
+ * graph, a process whose memory manager owns the device heap).  Arguments and
+ * results are pa_decode's, without the workspace: the split-KV scratch comes
+ * from a 16 MiB array inside the library that every device loading the
+ * library holds until the process exits.  The call allocates nothing.
+ *   - A batch whose plan needs more than 16 MiB of scratch (see
+ *     pa_decode_workspace_size) is rejected with PA_ERR_WORKSPACE before
+ *     anything is enqueued.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device); make that first call before any stream capture.
+ *   - Every call shares the array and it keeps the last call's contents;
+ *     nothing in it has to start at zero, but calls that overlap on the GPU
+ *     (two streams, two host threads) race on it.
+ */
+PA_API pa_status pa_decode_no_alloc(const pa_cache_desc* desc, const void* q, int32_t batch,
+                                    const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                    int32_t max_pages_per_seq, const int32_t* context_lens,
+                                    int32_t max_context_len, float scale, int32_t max_ctas, void* out,
+                                    pa_stream_t stream);
+
+/*
  * pa_prefill_varlen -- chunked-prefill attention for packed new tokens.
  *
  * Request b's chunk is rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q (flat

@@ -80,6 +80,7 @@ _SIGS = {
     "pa_decode_plan_info": (_I32, [_DESC, _I32, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "pa_decode": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP, ctypes.c_size_t,
                          _VP]),
+    "pa_decode_no_alloc": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP]),
     "pa_prefill_varlen": (_I32, [_DESC, _VP, _VP, _I32, _I32, _I64, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _VP, _VP]),
     "pa_validate_metadata": (_I32, [_DESC, _I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP]),
     "pa_selftest_bounded_wait": (_I32, [_I32, _VP]),
@@ -180,6 +181,15 @@ def pa_decode(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq,
         ctypes.byref(desc), _ptr(q), batch, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_pages_per_seq,
         _ptr(context_lens), max_context_len, scale, max_ctas, _ptr(out), _ptr(workspace), workspace_bytes,
         _stream(stream)))
+
+
+def pa_decode_no_alloc(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens,
+                       max_context_len, scale, max_ctas, out, stream=None):
+    """pa_decode with the library's fixed 16 MiB scratch instead of a caller workspace."""
+    lib = load_library()
+    _check("pa_decode_no_alloc", lib.pa_decode_no_alloc(
+        ctypes.byref(desc), _ptr(q), batch, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_pages_per_seq,
+        _ptr(context_lens), max_context_len, scale, max_ctas, _ptr(out), _stream(stream)))
 
 
 def pa_prefill_varlen(desc, q, cu_seqlens_q, batch, max_seqlen_q, num_tokens, k_cache, v_cache, block_tables,
