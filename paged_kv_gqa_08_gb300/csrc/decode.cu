@@ -36,7 +36,7 @@ namespace {
 constexpr int kTPL = 4;          // tokens per lane per chunk
 constexpr int kStages = 3;       // shared-memory ring depth
 constexpr int kPlanThreads = 1024;
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 
 __host__ __device__ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
 __host__ __device__ constexpr int pow2ceil(int x) { return x <= 1 ? 1 : 2 * pow2ceil((x + 1) / 2); }
@@ -201,7 +201,9 @@ PA_DEVINL void drain_wait(uint64_t* bar, uint32_t parity) {
 // the split-KV decode kernel
 // ---------------------------------------------------------------------------
 template <typename T, int HD, int G>
-__global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 112 : 168) decode_kernel(const KParams p) {
+// Register cap: a 9-warp CTA is charged as 10 warps, so two CTAs per SM need
+// at most 96 registers per thread (G <= 4); larger groups run one CTA per SM.
+__global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_kernel(const KParams p) {
   using Gm = Geom<T, HD>;
   constexpr int LPR = Gm::LPR, RPI = Gm::RPI, NPR = Gm::NPR;
   constexpr int V = G * kTPL;
@@ -473,54 +475,74 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 112 : 168) decode
 }
 
 // ---------------------------------------------------------------------------
-// log-sum-exp merge of the partials of requests cut across CTAs
+// log-sum-exp merge of the partials of requests cut across CTAs.  One warp per
+// (request, q-head); a lane owns HD/32 elements of the head; the loop over the
+// partials keeps several independent loads in flight.
 // ---------------------------------------------------------------------------
 template <typename T, int HD>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const KParams p) {
-  const int b = blockIdx.x;
+  constexpr int EL = HD / 32;  // elements per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + warp;
+  if (u >= static_cast<int64_t>(p.B) * p.Hq) return;
+  const int b = static_cast<int>(u / p.Hq), hq = static_cast<int>(u - static_cast<int64_t>(b) * p.Hq);
   const int NC = p.cs[p.B];
   const int cb0 = p.cs[b], cb1 = p.cs[b + 1];
   if (cb1 <= cb0) return;
-  auto owner = [&](int x) {
-    return static_cast<int>(((static_cast<int64_t>(x) + 1) * p.n_ctas + NC - 1) / NC) - 1;
-  };
-  const int c0 = owner(cb0), c1 = owner(cb1 - 1);
+  auto start = [&](int c) { return (static_cast<int64_t>(c) * NC) / p.n_ctas; };
+  const int c0 = static_cast<int>(((static_cast<int64_t>(cb0) + 1) * p.n_ctas + NC - 1) / NC) - 1;
+  const int c1 = static_cast<int>(((static_cast<int64_t>(cb1)) * p.n_ctas + NC - 1) / NC) - 1;
   if (c0 == c1) return;  // written whole by its CTA
   // With more CTAs than chunks some CTAs between c0 and c1 own no chunk and
   // wrote no partial: only CTAs with a non-empty range take part.
-  auto busy = [&](int c) {
-    return (static_cast<int64_t>(c) * NC) / p.n_ctas < (static_cast<int64_t>(c + 1) * NC) / p.n_ctas;
-  };
-  constexpr int D4 = HD / 4;
-  for (int idx = threadIdx.x; idx < p.Hq * D4; idx += blockDim.x) {
-    const int hq = idx / D4, d4 = idx - hq * D4;
-    float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc)
-      if (busy(cc)) M = fmaxf(M, p.lse_part[(static_cast<int64_t>(cc) + b) * p.Hq + hq]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (M != -INFINITY) {
-      for (int cc = c0; cc <= c1; ++cc) {
-        if (!busy(cc)) continue;
-        const int64_t slot = static_cast<int64_t>(cc) + b;
-        const float w = exp2f(p.lse_part[slot * p.Hq + hq] - M);
-        const float4 ov = *reinterpret_cast<const float4*>(p.o_part + (slot * p.Hq + hq) * HD + d4 * 4);
-        acc.x += w * ov.x;
-        acc.y += w * ov.y;
-        acc.z += w * ov.z;
-        acc.w += w * ov.w;
-        wsum += w;
+  float M = -INFINITY;
+  for (int cc = c0 + lane; cc <= c1; cc += 32)
+    if (start(cc) < start(cc + 1)) M = fmaxf(M, p.lse_part[(static_cast<int64_t>(cc) + b) * p.Hq + hq]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[EL];
+#pragma unroll
+  for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    int64_t s_lo = start(c0);
+#pragma unroll 4
+    for (int cc = c0; cc <= c1; ++cc) {
+      const int64_t s_hi = start(cc + 1);
+      const bool busy = s_lo < s_hi;
+      s_lo = s_hi;
+      if (!busy) continue;
+      const int64_t slot = static_cast<int64_t>(cc) + b;
+      const float w = exp2f(p.lse_part[slot * p.Hq + hq] - M);
+      const float* src = p.o_part + (slot * p.Hq + hq) * HD + lane * EL;
+      if constexpr (EL == 4) {
+        const float4 ov = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * ov.x;
+        acc[1] += w * ov.y;
+        acc[2] += w * ov.z;
+        acc[3] += w * ov.w;
+      } else {
+        const float2 ov = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * ov.x;
+        acc[1] += w * ov.y;
       }
+      wsum += w;
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int64_t e = (static_cast<int64_t>(b) * p.Hq + hq) * HD + d4 * 4;
-    if constexpr (sizeof(T) == 2) {
-      uint2 w;
-      w.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      w.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(p.out + e * 2) = w;
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int64_t e0 = (static_cast<int64_t>(b) * p.Hq + hq) * HD + lane * EL;
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (EL == 4) {
+      *reinterpret_cast<uint2*>(p.out + e0 * 2) =
+          make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
     } else {
-      *reinterpret_cast<float4*>(p.out + e * 4) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint32_t*>(p.out + e0 * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+  } else {
+    if constexpr (EL == 4) {
+      *reinterpret_cast<float4*>(p.out + e0 * 4) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    } else {
+      *reinterpret_cast<float2*>(p.out + e0 * 4) = make_float2(acc[0] * inv, acc[1] * inv);
     }
   }
 }
@@ -580,6 +602,9 @@ cudaError_t ctas_per_sm(const DeviceInfo& di, const void* fn, int threads, size_
   // opt-in maximum so every plan's shared-memory size fits.
   cudaError_t e =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
+  if (e != cudaSuccess) return e;
+  // Prefer the largest shared-memory carve-out so that several CTAs fit.
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int n = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
@@ -699,7 +724,9 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   cudaError_t e = cudaLaunchKernel(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), args, pl.smem_bytes, s);
   if (e != cudaSuccess) return e;
   if (pl.n_ctas > 1) {
-    e = cudaLaunchKernel(f.merge, dim3(a.batch), dim3(kMergeThreads), args, 0, s);
+    const int64_t pairs = static_cast<int64_t>(a.batch) * d.num_q_heads;
+    const unsigned blocks = static_cast<unsigned>((pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
+    e = cudaLaunchKernel(f.merge, dim3(blocks), dim3(kMergeThreads), args, 0, s);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
