@@ -237,6 +237,7 @@ PA_API pa_status pa_decode_no_alloc(const pa_cache_desc* desc, const void* q, in
  *   cu_seqlens_q     int32 [batch+1] as in pa_slot_mapping; num_tokens = cu[batch].
  *   max_seqlen_q     host upper bound on n_b.
  *   context_lens     int32 [batch], n_b <= context_lens[b] <= max_context_len.
+ *   scale            softmax scale (host), finite and > 0.
  *   out              [num_tokens, num_q_heads, head_dim] contiguous.
  * bf16 with head_dim 128 runs on the tcgen05 tensor cores; other cases on a
  * CUDA-core kernel.

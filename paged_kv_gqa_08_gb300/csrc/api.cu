@@ -288,7 +288,7 @@ pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int3
   if (max_pages_per_seq < 1 || max_context_len < 1 || max_seqlen_q > max_context_len) return PA_ERR_SHAPE;
   if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * desc->page_size)
     return PA_ERR_SHAPE;
-  if (!isfinite(scale)) return PA_ERR_SHAPE;
+  if (!isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
   if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
   unsigned int* err = nullptr;

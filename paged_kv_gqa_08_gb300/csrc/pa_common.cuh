@@ -143,6 +143,14 @@ PA_DEVINL float2 ffma2(float2 a, float2 b, float2 c) {
   return *reinterpret_cast<float2*>(&d);
 }
 
+PA_DEVINL float2 fadd2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 PA_DEVINL float2 fmul2(float2 a, float2 b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;"
@@ -167,7 +175,9 @@ PA_DEVINL uint16_t float_to_bf16_bits(float x) {
 }
 
 PA_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(float_to_bf16_bits(lo)) | (static_cast<uint32_t>(float_to_bf16_bits(hi)) << 16);
+  // one cvt.rn.bf16x2.f32: hi goes to the upper half
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // Round a float to the storage dtype's value set (identity for fp32).

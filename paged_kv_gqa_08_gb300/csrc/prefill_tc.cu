@@ -7,23 +7,30 @@
 // chunk sits at position context_lens[b] - n_b + i and attends to keys
 // 0 .. that position, all read from the paged cache.
 //
-// One CTA = (request, kv-head, q-tile).  The 128 rows of a tile are
-// TQ = 128 / G tokens x the G q-heads that share the kv-head, so every K/V
-// tile staged in shared memory feeds the whole GQA group.
-//   warp 0     TMA producer: Q once (3-D map), then per 128-key tile the K and
-//              V rows, gathered page by page with 16-row boxes (single-row
-//              boxes for a ragged end, so no slot past the context is read).
-//   warp 1     allocates 512 TMEM columns; lane 0 issues the MMAs:
-//              S[j%2] = Q K_j^T (two S buffers in TMEM) and O += P_j V_j.
-//   warps 2-5  softmax, one thread per row (= TMEM lane): scale, causal
-//              mask, base-2 online softmax with lazy rescaling (O in TMEM is
-//              rescaled only when a row max grows by more than 2^8), P as bf16
-//              into 128B-swizzled shared memory, final O / l to global memory.
+// One CTA = (request, kv-head, pair of q-tiles).  A q-tile is 128 rows:
+// TQ = 128 / G tokens x the G q-heads that share the kv-head, so each staged
+// K/V tile feeds the whole GQA group, and it feeds both q-tiles of the pair
+// (256 rows per K/V tile).
+//   warp 0     TMA producer: both Q tiles once (3-D map), then per 128-key tile
+//              the K and V rows gathered page by page with 16-row boxes
+//              (single-row boxes for a ragged end, so no slot past the context
+//              is read).
+//   warp 1     allocates all 512 TMEM columns; lane 0 issues the MMAs:
+//              S_g = Q_g K_j^T and O_g += P_g V_j for the two q-tiles g, in
+//              the order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), so that each
+//              softmax group has a PV and a QK of the other group to hide in.
+//   warps 2-9  two softmax groups of 4 warps, one thread per row (= TMEM
+//              lane): pass 1 reads S and takes the row max; O in TMEM is
+//              rescaled only when a row max grows by more than 2^8; pass 2
+//              reads S again, turns it into bf16 probabilities and writes them
+//              back over S's first 64 columns, where the PV MMA reads its A
+//              operand.  Finally O / l goes to global memory.
+// TMEM: S_0 cols 0-127 (P_0 in 0-63), S_1 128-255 (P_1 in 128-191),
+//       O_0 256-383, O_1 384-511.
 // Every wait is bounded; a timeout raises PA_DEVERR_TIMEOUT and the CTA
 // drains its copies and MMAs, frees its TMEM and returns.
 #include <cuda.h>
 #include <math.h>
-
 #include <string.h>
 
 #include <mutex>
@@ -33,20 +40,18 @@
 namespace pa {
 namespace {
 
-constexpr int kBM = 128;                    // rows per tile
+constexpr int kBM = 128;                    // rows per q-tile
 constexpr int kBN = 128;                    // keys per tile
 constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 bf16 (one swizzle-atom column)
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kBoxRows = 16;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;  // S0 at 0, S1 at 128, O at 256
 
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + 2 * kTileBytes;
-constexpr int kOffP = kOffV + 2 * kTileBytes;
-constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kOffQ = 0;                          // two q-tiles
+constexpr int kOffK = kOffQ + 2 * kTileBytes;     // two K stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;     // two V stages
+constexpr int kOffBar = kOffV + 2 * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + slack to align the base to 1024
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, M = 128, N = 128.
@@ -152,6 +157,33 @@ PA_DEVINL void drain(uint64_t* bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitLimitNs) return;
 }
 
+
+// O += A(TMEM) * B(smem): the A operand (probabilities) is read from tensor memory.
+PA_DEVINL void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+PA_DEVINL void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// 2^x on the special-function unit (PTX ex2.approx; inputs here are <= 8).
+PA_DEVINL float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -159,44 +191,49 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s0 = p.cu[b], s1 = p.cu[b + 1];
   const int n = s1 - s0;
-  if (qt * p.TQ >= n) return;
+  if (2 * qp * p.TQ >= n) return;
   const int L = p.ctx[b];
   const int cap = min(p.max_ctx, p.maxp << p.log2P);
   if (s0 < 0 || L < n || L > cap) {
     if (threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
     return;
   }
-  const int rows_t = min(p.TQ, n - qt * p.TQ);  // live tokens in this tile
-  const int pos0 = L - n + qt * p.TQ;           // position of its first token
-  const int kv_len = pos0 + rows_t;             // keys the tile needs
-  const int nt = (kv_len + kBN - 1) / kBN;
+  const int nq = (2 * qp + 1) * p.TQ < n ? 2 : 1;  // q-tiles of the pair with rows
+  int rows[2], pos0[2], ntg[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int qt = 2 * qp + g;
+    rows[g] = g < nq ? min(p.TQ, n - qt * p.TQ) : 0;   // live tokens of the tile
+    pos0[g] = L - n + qt * p.TQ;                       // position of its first token
+    ntg[g] = g < nq ? (pos0[g] + rows[g] + kBN - 1) / kBN : 0;  // key tiles it needs
+  }
+  const int kv_len = pos0[nq - 1] + rows[nq - 1];
+  const int nt = ntg[nq - 1];
 
-  unsigned char* sQ = smem + kOffQ;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = bars + 3;
   uint64_t* k_empty = bars + 5;
   uint64_t* v_empty = bars + 7;
-  uint64_t* s_full = bars + 9;
-  uint64_t* s_free = bars + 11;
-  uint64_t* p_full = bars + 13;
-  uint64_t* pv_done = bars + 15;
-  uint64_t* o_final = bars + 17;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18) + 1;
+  uint64_t* s_full = bars + 9;    // per q-tile
+  uint64_t* p_full = bars + 11;   // per q-tile
+  uint64_t* pv_done = bars + 13;  // per q-tile
+  uint64_t* o_final = bars + 15;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16) + 1;
 
-  // Rows never loaded must hold finite values: zero Q and both V stages.
+  // Rows never loaded must hold finite values: zero both Q tiles and both V stages.
   {
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < kTileBytes / 16; i += kThreads)
+    for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads) {
       reinterpret_cast<uint4*>(smem + kOffQ)[i] = z;
-    for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads)
       reinterpret_cast<uint4*>(smem + kOffV)[i] = z;
+    }
   }
   fence_async_smem();
   if (threadIdx.x == 0) {
@@ -207,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 4);
       mbar_init(&p_full[s], 4);
       mbar_init(&pv_done[s], 1);
     }
@@ -231,9 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     int issued_k = 0, issued_v = 0;
     bool ok = true;
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(2 * p.G * p.TQ * 128));
-      tma_load_3d(sQ, &p.tm_q, 0, h * p.G, s0 + qt * p.TQ, q_full);
-      tma_load_3d(sQ + kHalfBytes, &p.tm_q, 64, h * p.G, s0 + qt * p.TQ, q_full);
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nq * 2 * p.G * p.TQ * 128));
+      for (int g = 0; g < nq; ++g) {
+        const int z = s0 + (2 * qp + g) * p.TQ;
+        tma_load_3d(smem + kOffQ + g * kTileBytes, &p.tm_q, 0, h * p.G, z, q_full);
+        tma_load_3d(smem + kOffQ + g * kTileBytes + kHalfBytes, &p.tm_q, 64, h * p.G, z, q_full);
+      }
     }
     const int64_t bt_row = static_cast<int64_t>(b) * p.maxp;
     const int box = lane >> 2, half = (lane >> 1) & 1, isv = lane & 1;
@@ -264,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         kb += __shfl_xor_sync(0xffffffffu, kb, o);
         vb += __shfl_xor_sync(0xffffffffu, vb, o);
       }
-      // K of tile j (stage freed by QK_{j-2})
       int okk = 1;
       if (lane == 0) {
         okk = mbar_wait_bounded(&k_empty[st], par, abort_flag, p.err);
@@ -279,7 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, &p.tm_k1, x, y_rem + r, &k_full[st]);
       }
       ++issued_k;
-      // V of tile j (stage freed by PV_{j-2})
       int okv = 1;
       if (lane == 0) {
         okv = mbar_wait_bounded(&v_empty[st], par, abort_flag, p.err);
@@ -304,154 +341,161 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag, p.err);
-      const uint32_t aQ = smem_u32(sQ);
-      const uint32_t aK = smem_u32(smem + kOffK), aV = smem_u32(smem + kOffV), aP = smem_u32(smem + kOffP);
-      auto qk = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&k_full[st], (j >> 1) & 1, abort_flag, p.err)) return false;
-        if (j >= 2 && !mbar_wait_bounded(&s_free[st], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t kbase = aK + st * kTileBytes;
+      const uint32_t aQ = smem_u32(smem + kOffQ);
+      const uint32_t aK = smem_u32(smem + kOffK), aV = smem_u32(smem + kOffV);
+      auto qk = [&](int g, int j) {
+        const uint32_t qbase = aQ + g * kTileBytes, kbase = aK + (j & 1) * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          mma_bf16(tmem + st * kBN, sdesc(aQ + off, 16, 1024), sdesc(kbase + off, 16, 1024), kIdescQK, k > 0);
+          mma_bf16(tmem + g * 128, sdesc(qbase + off, 16, 1024), sdesc(kbase + off, 16, 1024), kIdescQK, k > 0);
         }
-        mma_commit(&k_empty[st]);
-        mma_commit(&s_full[st]);
-        return true;
+        mma_commit(&s_full[g]);
       };
-      auto pv = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&p_full[st], (j >> 1) & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait_bounded(&v_full[st], (j >> 1) & 1, abort_flag, p.err)) return false;
+      auto pv = [&](int g, int j) -> bool {
+        if (!mbar_wait_bounded(&p_full[g], j & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t pbase = aP + st * kTileBytes, vbase = aV + st * kTileBytes;
+        const uint32_t vbase = aV + (j & 1) * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t a = sdesc(pbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc(vbase + k * 16 * 128, kHalfBytes, 1024);
-          mma_bf16(tmem + kColO, a, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(&v_empty[st]);
-        mma_commit(&pv_done[st]);
+        for (int k = 0; k < 8; ++k)
+          mma_bf16_ts(tmem + 256 + g * 128, tmem + g * 128 + k * 8, sdesc(vbase + k * 16 * 128, kHalfBytes, 1024),
+                      kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&pv_done[g]);
         return true;
       };
-      if (ok) ok = qk(0);
-      for (int j = 1; j < nt && ok; ++j) {
-        ok = qk(j);
-        if (ok) ok = pv(j - 1);
+      if (ok) ok = mbar_wait_bounded(&k_full[0], 0, abort_flag, p.err);
+      if (ok) {
+        tc_fence_after();
+        for (int g = 0; g < nq; ++g) qk(g, 0);
+        mma_commit(&k_empty[0]);
       }
-      if (ok) ok = pv(nt - 1);
+      for (int j = 0; j < nt && ok; ++j) {
+        const bool more = j + 1 < nt;
+        if (!(ok = mbar_wait_bounded(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.err))) break;
+        // q-tile 0: PV of tile j, then QK of tile j+1 (the tensor pipe runs them
+        // in issue order, so QK overwrites S_0 only after PV has read P_0)
+        if (j < ntg[0] && !(ok = pv(0, j))) break;
+        if (more) {
+          if (!(ok = mbar_wait_bounded(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          if (j + 1 < ntg[0]) qk(0, j + 1);
+        }
+        // q-tile 1
+        if (j < ntg[1] && !(ok = pv(1, j))) break;
+        if (more && j + 1 < ntg[1]) qk(1, j + 1);
+        mma_commit(&v_empty[j & 1]);
+        if (more) mma_commit(&k_empty[(j + 1) & 1]);
+      }
       mma_commit(o_final);
       if (!ok) drain(o_final, 0);
     }
   } else {
-    // ------------------------------- softmax -------------------------------
-    const int wq = warp & 3;
+    // ------------------------------- softmax groups -------------------------------
+    const int g = (warp - 2) >> 2;
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const int t = row / p.G, g = row - (row / p.G) * p.G;
-    const bool live = row < p.TQ * p.G && t < rows_t;
-    const int pos_r = pos0 + t;
+    const uint32_t colS = g * 128, colO = 256 + g * 128;
+    const int t = row / p.G, gg = row - (row / p.G) * p.G;
+    const bool live = g < nq && row < p.TQ * p.G && t < rows[g];
+    const int pos_r = pos0[g] + t;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int st = j & 1;
-      ok = mbar_wait_bounded(&s_full[st], (j >> 1) & 1, abort_flag, p.err);
+    for (int j = 0; j < ntg[g]; ++j) {
+      ok = mbar_wait_bounded(&s_full[g], j & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float x[kBN];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + st * kBN + 32 * c, reinterpret_cast<uint32_t*>(x) + 32 * c);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-
       const int key0 = j * kBN;
-      const bool need_mask = key0 + kBN - 1 > pos0;
-      float mx = -INFINITY;
+      const bool need_mask = key0 + kBN - 1 > pos0[g];
+      // pass 1: row max of the raw scores (the scale is positive, so it
+      // commutes with the max)
+      float mraw = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_off + colS + 32 * c, x);
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        float v = x[c] * p.scale_log2;
-        if (need_mask && key0 + c > pos_r) v = -INFINITY;
-        x[c] = v;
-        mx = fmaxf(mx, v);
+        for (int e = 0; e < 32; ++e) {
+          float v = __uint_as_float(x[e]);
+          if (need_mask && key0 + 32 * c + e > pos_r) v = -INFINITY;
+          mraw = fmaxf(mraw, v);
+        }
       }
+      const float mx = mraw * p.scale_log2;
       if (__any_sync(0xffffffffu, mx > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, mx);
-        const float alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - m_new);
+        const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
         if (j > 0) {
-          ok = mbar_wait_bounded(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err);
+          ok = mbar_wait_bounded(&pv_done[g], (j - 1) & 1, abort_flag, p.err);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+            tmem_ld32(tmem + lane_off + colO + 32 * c, o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_off + kColO + 32 * c, o);
+            tmem_st32(tmem + lane_off + colO + 32 * c, o);
           }
           tmem_wait_st();
         }
         l *= alpha;
         m_used = m_new;
       }
-      // P buffer st was last read by PV_{j-2}
-      if (j >= 2) {
-        ok = mbar_wait_bounded(&pv_done[st], ((j >> 1) & 1) ^ 1, abort_flag, p.err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      }
-      unsigned char* pb = smem + kOffP + st * kTileBytes + row * 128;
-      float rsum = 0.f;
+      // pass 2: probabilities as bf16, written over the first 64 columns of S
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+      float2 rsum = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_off + colS + 32 * c, x);
+        uint32_t w[16];
 #pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(x[c16 * 8 + 2 * e] - m_used);
-          const float p1 = exp2f(x[c16 * 8 + 2 * e + 1] - m_used);
-          rsum += p0 + p1;
+        for (int e = 0; e < 16; ++e) {
+          float p0 = ex2(fmaf(__uint_as_float(x[2 * e]), p.scale_log2, neg_m));
+          float p1 = ex2(fmaf(__uint_as_float(x[2 * e + 1]), p.scale_log2, neg_m));
+          if (need_mask) {
+            if (key0 + 32 * c + 2 * e > pos_r) p0 = 0.f;
+            if (key0 + 32 * c + 2 * e + 1 > pos_r) p1 = 0.f;
+          }
+          rsum = fadd2(rsum, make_float2(p0, p1));
           w[e] = pack_bf16x2(p0, p1);
         }
-        const int hf = c16 >> 3, cc = c16 & 7;
-        *reinterpret_cast<uint4*>(pb + hf * kHalfBytes + ((cc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st16(tmem + lane_off + colS + 16 * c, w);
       }
-      l += rsum;
-      fence_async_smem();
+      tmem_wait_st();
+      l += rsum.x + rsum.y;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[st]);
+      if (lane == 0) mbar_arrive(&p_full[g]);
     }
     // epilogue: O / l to global memory
-    if (ok) ok = mbar_wait_bounded(o_final, 0, abort_flag, p.err);
-    if (__all_sync(0xffffffffu, ok)) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      char* dst = p.out + ((static_cast<int64_t>(s0) + qt * p.TQ + t) * p.Hq + h * p.G + g) * 256;
+    if (g < nq) {
+      if (ok) ok = mbar_wait_bounded(o_final, 0, abort_flag, p.err);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        char* dst = p.out + ((static_cast<int64_t>(s0) + (2 * qp + g) * p.TQ + t) * p.Hq + h * p.G + gg) * 256;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + colO + 32 * c, o);
+          if (live) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
-        if (live) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 64 + q4 * 16) = w;
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c * 64 + q4 * 16) = w;
+            }
           }
         }
       }
@@ -556,7 +600,8 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
       done[dev] = true;
     }
   }
-  const dim3 grid((a.max_seqlen_q + TQ - 1) / TQ, d.num_kv_heads, a.batch);
+  const int qtiles = (a.max_seqlen_q + TQ - 1) / TQ;
+  const dim3 grid((qtiles + 1) / 2, d.num_kv_heads, a.batch);
   prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }

@@ -136,6 +136,8 @@ def test_prefill_argument_validation(lib):
     assert call(cu=None) == pa.PA_ERR_NULL
     assert call(maxq=200) == pa.PA_ERR_SHAPE      # longer than max_context_len
     assert call(max_ctx=200) == pa.PA_ERR_SHAPE   # beyond max_pages * page_size
+    assert lib.pa_prefill_varlen(ctypes.byref(d), FAKE, FAKE, 2, 64, 100, FAKE, FAKE, FAKE, 8, FAKE, 128, -0.1,
+                                 FAKE, None) == pa.PA_ERR_SHAPE       # the scale must be positive
 
 
 def test_slot_mapping_and_validate_argument_validation(lib):

@@ -83,3 +83,15 @@ def test_prefill_empty_requests_in_batch():
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
     _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+
+
+def test_mixed_decode_rows_and_prefill_chunks_in_one_launch():
+    # decode requests are chunks of length 1 in the same varlen batch as real chunks
+    spec = dict(kind="prefill", dtype="bf16", B=6, Hq=32, Hkv=8, hd=128, P=16, chunks=[1, 300, 1, 1, 77, 1],
+                prefixes=[900, 0, 45, 2047, 129, 3], norm=True, seed=21)
+    wl = synth.make_workload(spec)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
