@@ -167,6 +167,28 @@ PA_DEVINL void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, ui
       : "memory");
 }
 
+// Load 32 columns without waiting; the registers are valid only after
+// tmem_wait_ld32 on the same array, whose asm reads and rewrites them so the
+// compiler cannot move any use above the wait.
+PA_DEVINL void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : PA_R32(r)
+      : "r"(taddr)
+      : "memory");
+}
+
+#define PA_RW32(r)                                                                                              \
+  "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), \
+      "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),  \
+      "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), \
+      "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+
+PA_DEVINL void tmem_wait_ld32(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PA_RW32(r)::"memory");
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane.
 PA_DEVINL void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -411,20 +433,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int key0 = j * kBN;
       const bool need_mask = key0 + kBN - 1 > pos0[g];
       // pass 1: row max of the raw scores (the scale is positive, so it
-      // commutes with the max)
-      float mraw = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tmem + lane_off + colS + 32 * c, x);
+      // commutes with the max).  All four loads are issued before one wait;
+      // eight independent accumulators keep the max off a serial chain.
+      float mx;
+      {
+        uint32_t x[128];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(x[e]);
-          if (need_mask && key0 + 32 * c + e > pos_r) v = -INFINITY;
-          mraw = fmaxf(mraw, v);
+        for (int c = 0; c < 4; ++c) tmem_ld32_async(tmem + lane_off + colS + 32 * c, x + 32 * c);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_wait_ld32(x + 32 * c);
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e)
+            m8[e & 7] = fmaxf(m8[e & 7], key0 + e > pos_r ? -INFINITY : __uint_as_float(x[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(x[e]));
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
+        mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])) * p.scale_log2;
       }
-      const float mx = mraw * p.scale_log2;
       if (__any_sync(0xffffffffu, mx > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, mx);
         const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
@@ -449,27 +481,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         m_used = m_new;
       }
       // pass 2: probabilities as bf16, written over the first 64 columns of S
+      // (half h reads columns 64h..64h+63 and writes 32h..32h+31, which hold
+      // scores already consumed).
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-      float2 rsum = make_float2(0.f, 0.f);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tmem + lane_off + colS + 32 * c, x);
-        uint32_t w[16];
+      float2 rs4[4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < 4; ++e) rs4[e] = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t x[64];
+        tmem_ld32_async(tmem + lane_off + colS + 64 * hh, x);
+        tmem_ld32_async(tmem + lane_off + colS + 64 * hh + 32, x + 32);
+        tmem_wait_ld32(x);
+        tmem_wait_ld32(x + 32);
+        uint32_t w[32];
+        const int kb = key0 + 64 * hh;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
           float p0 = ex2(fmaf(__uint_as_float(x[2 * e]), p.scale_log2, neg_m));
           float p1 = ex2(fmaf(__uint_as_float(x[2 * e + 1]), p.scale_log2, neg_m));
           if (need_mask) {
-            if (key0 + 32 * c + 2 * e > pos_r) p0 = 0.f;
-            if (key0 + 32 * c + 2 * e + 1 > pos_r) p1 = 0.f;
+            if (kb + 2 * e > pos_r) p0 = 0.f;
+            if (kb + 2 * e + 1 > pos_r) p1 = 0.f;
           }
-          rsum = fadd2(rsum, make_float2(p0, p1));
+          rs4[e & 3] = fadd2(rs4[e & 3], make_float2(p0, p1));
           w[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + lane_off + colS + 16 * c, w);
+        tmem_st16(tmem + lane_off + colS + 32 * hh, w);
+        tmem_st16(tmem + lane_off + colS + 32 * hh + 16, w + 16);
       }
       tmem_wait_st();
+      const float2 rsum = fadd2(fadd2(rs4[0], rs4[1]), fadd2(rs4[2], rs4[3]));
       l += rsum.x + rsum.y;
       tc_fence_before();
       __syncwarp();
