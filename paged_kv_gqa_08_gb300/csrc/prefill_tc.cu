@@ -432,27 +432,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       tc_fence_after();
       const int key0 = j * kBN;
       const bool need_mask = key0 + kBN - 1 > pos0[g];
-      // pass 1: row max of the raw scores (the scale is positive, so it
-      // commutes with the max).  All four loads are issued before one wait;
-      // eight independent accumulators keep the max off a serial chain.
+      // One TMEM round trip per tile: all 128 scores of the row are loaded
+      // (four loads, one wait), the row max is taken over the raw scores (the
+      // scale is positive, so it commutes with the max) with eight independent
+      // accumulators, and the probabilities are computed from registers.
+      uint32_t x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32_async(tmem + lane_off + colS + 32 * c, x + 32 * c);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_wait_ld32(x + 32 * c);
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (key0 + e > pos_r) x[e] = __float_as_uint(-INFINITY);
+      }
       float mx;
       {
-        uint32_t x[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_async(tmem + lane_off + colS + 32 * c, x + 32 * c);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_wait_ld32(x + 32 * c);
         float m8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-        if (need_mask) {
+        for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
-            m8[e & 7] = fmaxf(m8[e & 7], key0 + e > pos_r ? -INFINITY : __uint_as_float(x[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(x[e]));
-        }
+        for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(x[e]));
 #pragma unroll
         for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
         mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])) * p.scale_log2;
@@ -480,30 +480,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         l *= alpha;
         m_used = m_new;
       }
-      // pass 2: probabilities as bf16, written over the first 64 columns of S
-      // (half h reads columns 64h..64h+63 and writes 32h..32h+31, which hold
-      // scores already consumed).
+      // probabilities as bf16, written over the first 64 columns of S (masked
+      // scores are -inf and give exactly 0)
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       float2 rs4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) rs4[e] = make_float2(0.f, 0.f);
-#pragma unroll 1
+#pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t x[64];
-        tmem_ld32_async(tmem + lane_off + colS + 64 * hh, x);
-        tmem_ld32_async(tmem + lane_off + colS + 64 * hh + 32, x + 32);
-        tmem_wait_ld32(x);
-        tmem_wait_ld32(x + 32);
         uint32_t w[32];
-        const int kb = key0 + 64 * hh;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          float p0 = ex2(fmaf(__uint_as_float(x[2 * e]), p.scale_log2, neg_m));
-          float p1 = ex2(fmaf(__uint_as_float(x[2 * e + 1]), p.scale_log2, neg_m));
-          if (need_mask) {
-            if (kb + 2 * e > pos_r) p0 = 0.f;
-            if (kb + 2 * e + 1 > pos_r) p1 = 0.f;
-          }
+          const float p0 = ex2(fmaf(__uint_as_float(x[64 * hh + 2 * e]), p.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(x[64 * hh + 2 * e + 1]), p.scale_log2, neg_m));
           rs4[e & 3] = fadd2(rs4[e & 3], make_float2(p0, p1));
           w[e] = pack_bf16x2(p0, p1);
         }
