@@ -76,6 +76,13 @@ def write_bytes(wl) -> int:
     return b
 
 
+def fused_write_bytes(wl) -> int:
+    """The KV write inside pa_decode_kv_write: read the new k, v rows, write them
+    into the cache, write the slot of each request."""
+    row = wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    return 4 * wl.batch * row + 8 * wl.batch
+
+
 def prefill_flops(wl) -> int:
     """4 * head_dim * Hq * (unmasked query-key pairs): QK^T plus PV."""
     pairs = 0
@@ -213,9 +220,10 @@ def profiled_traffic(key: str, src_files) -> object:
 # device setup and timing
 # ---------------------------------------------------------------------------
 class Device:
-    def __init__(self, wl, dev, max_ctas=0):
+    def __init__(self, wl, dev, max_ctas=0, fused=False):
         self.wl = wl
         self.dev = dev
+        self.fused = fused and wl.kind == "decode"   # KV write fused into decode (pa_decode_kv_write)
         self.t = synth.to_torch(wl, dev)
         self.desc = cache_desc(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
                                PA_F32 if wl.dtype == "f32" else PA_BF16)
@@ -236,6 +244,8 @@ class Device:
         wl, t, b = self.wl, self.t, self.bufs
         from paged_kv_gqa_08_gb300 import pa_kv_write, pa_qk_norm_rope_kv_write, pa_slot_mapping
         n = wl.num_new_tokens
+        if self.fused:
+            return
         pa_slot_mapping(self.desc, wl.batch, t["cu_seqlens_q"], t["context_lens"], t["block_tables"],
                         wl.max_pages_per_seq, n, b.positions, b.slots)
         if wl.q_norm_w is not None:
@@ -250,7 +260,13 @@ class Device:
     def attn_part(self):
         wl, t, b = self.wl, self.t, self.bufs
         q = b.q_out if wl.q_norm_w is not None else t["q"]
-        if wl.kind == "decode":
+        if self.fused:
+            from paged_kv_gqa_08_gb300 import pa_decode_kv_write
+            row = wl.num_kv_heads * wl.head_dim
+            pa_decode_kv_write(self.desc, q, t["k_new"], row, t["v_new"], row, wl.batch, self.k_cache, self.v_cache,
+                               t["block_tables"], wl.max_pages_per_seq, t["context_lens"], wl.max_context_len,
+                               wl.scale, b.max_ctas, b.slots, b.out, b.workspace)
+        elif wl.kind == "decode":
             pa_decode(self.desc, q, wl.batch, self.k_cache, self.v_cache, t["block_tables"], wl.max_pages_per_seq,
                       t["context_lens"], wl.max_context_len, wl.scale, b.max_ctas, b.out, b.workspace)
         else:
@@ -308,6 +324,39 @@ def time_device_steps(d: Device, steps: int, warmup: int, world: int, clocks: Cl
     return max_over_ranks(total_ms, world), attn_ms, write_ms
 
 
+def capture_graph(body):
+    """Capture `body` (after one eager run, so every plan is cached) into a CUDA graph."""
+    body()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        body()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph_steps(d: Device, steps: int, warmup: int, world: int, clocks=None):
+    """The whole step as one CUDA graph, replayed back to back."""
+    g = capture_graph(lambda: (d.write_part(), d.attn_part()))
+    for _ in range(warmup):
+        g.replay()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ctx = clocks if clocks is not None else _Null()
+    with ctx:
+        start.record()
+        for _ in range(steps):
+            g.replay()
+        end.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(start.elapsed_time(end), world)
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -327,12 +376,18 @@ def time_e2e(d: Device, steps: int, warmup: int, world: int):
     out_host = torch.empty((n,) + tuple(d.bufs.out.shape[1:]), dtype=d.bufs.out.dtype).pin_memory()
     d2h = out_host.numel() * out_host.element_size()
 
-    def one():
+    def body():
         for k in names:
             t[k].copy_(host[k], non_blocking=True)
         d.write_part()
         d.attn_part()
         out_host.copy_(d.bufs.out[:n], non_blocking=True)
+
+    # copies in, the step, the result out: one graph launch and one host sync per step
+    g = capture_graph(body)
+
+    def one():
+        g.replay()
         torch.cuda.current_stream().synchronize()
 
     for _ in range(warmup):
@@ -427,6 +482,31 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+def run_case(spec: str):
+    """Profiling helper: set up the first B requests of a workload and run three
+    steps through the C ABI (no timing), e.g. --case decode:qwen3_8b_decode:16."""
+    kind, name, nreq = spec.split(":")
+    nreq = int(nreq)
+    c = synth.CONFIGS[name]
+    if nreq == c["B"]:
+        wl = synth.make_workload(name)
+    elif kind == "prefill":
+        extra = {"prefixes": c["prefixes"][:nreq]} if "prefixes" in c else {}
+        wl = synth.make_workload(name, B=nreq, chunks=c["chunks"][:nreq], **extra)
+    else:
+        wl = synth.make_workload(name, B=nreq)
+    pa_build.build()
+    load_library()
+    d = Device(wl, "cuda:0")
+    for _ in range(3):
+        d.write_part()
+        d.attn_part()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": spec, "workload": describe(wl), "kv_bytes": kv_bytes(wl),
+                      "decode_bytes": decode_call_bytes(wl) if wl.kind == "decode" else None,
+                      "prefill_flops": prefill_flops(wl) if wl.kind == "prefill" else None}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -435,7 +515,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="headline only (no prefill / other configs)")
+    ap.add_argument("--case", help="profiling helper KIND:CONFIG:B (see run_case); runs 3 steps and exits")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
@@ -460,37 +544,49 @@ def main():
 
     # ---------------- headline: decode step ----------------
     wl = synth.make_workload(HEADLINE)
-    d = Device(wl, dev)
+    # the same step with separate slot-mapping / KV-write / decode calls, for comparison
+    du = Device(wl, dev)
+    unfused_ms = time_graph_steps(du, args.steps, args.warmup, world) / args.steps
+    del du
+    torch.cuda.empty_cache()
+    d = Device(wl, dev, fused=True)
     clocks = ClockSampler(local)
-    total_ms, attn_ms, write_ms = time_device_steps(d, args.steps, args.warmup, world, clocks)
+    # per-call CUDA events (eager launches) give the kernel-level roofline numbers
+    eager_total_ms, attn_ms, write_ms = time_device_steps(d, args.steps, args.warmup, world)
+    # the timed steps: the whole step replayed as one CUDA graph
+    total_ms = time_graph_steps(d, args.steps, args.warmup, world, clocks)
     ms = total_ms / args.steps
-    step_bytes = decode_call_bytes(wl) + write_bytes(wl)
+    step_bytes = decode_call_bytes(wl) + fused_write_bytes(wl)
     value = whole_job_rate(step_bytes, ms, world) / 1e9
     tok_s = whole_job_rate(wl.batch, ms, world)
-    dec_bytes = decode_call_bytes(wl)
+    dec_bytes = step_bytes
     achieved = dec_bytes / (attn_ms * 1e-3) / 1e9
     traffic = profiled_traffic("decode_qwen3_0p6b", ["decode.cu", "pa_common.cuh"])
     e2e_ms, h2d, d2h = time_e2e(d, max(20, args.steps // 5), args.warmup, world)
     e2e_step_ms = e2e_ms / max(20, args.steps // 5)
     from paged_kv_gqa_08_gb300 import pa_decode_plan_info
     n_parts, _ = pa_decode_plan_info(d.desc, wl.batch, wl.max_context_len, 0)
-    # per step: slot mapping, KV write, decode plan, split-KV decode, merge (if split)
-    launches = args.steps * (4 + (1 if n_parts > 1 else 0))
+    # per step: decode plan, split-KV decode with the KV write, merge (if split)
+    launches = args.steps * (2 + (1 if n_parts > 1 else 0))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic (seeded, synth/)",
-        "config": {"workload": describe(wl), "step": "slot mapping + KV write + split-KV decode + LSE merge",
+        "config": {"workload": describe(wl), "step": "slot mapping and KV write fused into split-KV decode "
+                   "(pa_decode_kv_write) + LSE merge, launched as one CUDA graph",
                    "global_batch": world * wl.batch, "kv_bytes_per_step": kv_bytes(wl),
                    "algorithmic_bytes_per_step": step_bytes, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV cache 1.1 GB > 129 MB L2); no flush"},
         "attn_tok_per_s": tok_s,
         "hbm_frac_of_step": value / world / hbm_peak,
-        "roofline": {"kernel": "pa_decode (plan + split-KV decode + merge kernels)", "bound": "hbm",
+        "roofline": {"kernel": "pa_decode_kv_write (plan + split-KV decode with KV write + merge kernels)",
+                     "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic, "peak_source": f"hbm_gbs of {peak_src}",
                      "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": attn_ms},
         "write_part_ms": write_ms,
+        "eager_ms_per_step": eager_total_ms / args.steps,
+        "unfused_ms_per_step": unfused_ms,
         "e2e": {"value": world * step_bytes / (e2e_step_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
         "gpu_launches": launches,

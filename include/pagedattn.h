@@ -197,6 +197,32 @@ PA_API pa_status pa_decode(const pa_cache_desc* desc, const void* q, int32_t bat
                     pa_stream_t stream);
 
 /*
+ * pa_decode_kv_write -- the decode step's KV write and decode attention in one
+ * launch sequence: for each request b, row b of k_new / v_new is stored into
+ * the slot of position context_lens[b] - 1 (the slot pa_slot_mapping gives:
+ * block_tables[b][pos / page_size] * page_size + pos % page_size) and the
+ * request's query attends to its context_lens[b] keys, the new one included
+ * (nano-vLLM learning note, Attention.forward: store the new K/V, then
+ * attend).  Equal to pa_slot_mapping + pa_kv_write + pa_decode, bit for bit
+ * in the cache and the output, without their two extra launches: the new row
+ * is read straight from k_new / v_new and stored by the CTA that attends to it.
+ *
+ *   k_new, v_new     [batch, num_kv_heads, head_dim] rows at k_row_stride /
+ *                    v_row_stride (elements, 16-byte multiples).
+ *   slot_mapping     optional int64 [batch] out: the slot written for each
+ *                    request, -1 for a request skipped for bad metadata.
+ *   other arguments  as pa_decode; the workspace size is pa_decode's.
+ * Needs num_pages * page_size < 2^31 (else PA_ERR_UNSUPPORTED).
+ */
+PA_API pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, const void* k_new,
+                                    int64_t k_row_stride, const void* v_new, int64_t v_row_stride,
+                                    int32_t batch, void* k_cache, void* v_cache, const int32_t* block_tables,
+                                    int32_t max_pages_per_seq, const int32_t* context_lens,
+                                    int32_t max_context_len, float scale, int32_t max_ctas,
+                                    int64_t* slot_mapping, void* out, void* workspace,
+                                    size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_no_alloc -- pa_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart of this call.
  *

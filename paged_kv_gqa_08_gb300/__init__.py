@@ -80,6 +80,8 @@ _SIGS = {
     "pa_decode_plan_info": (_I32, [_DESC, _I32, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "pa_decode": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP, ctypes.c_size_t,
                          _VP]),
+    "pa_decode_kv_write": (_I32, [_DESC, _VP, _VP, _I64, _VP, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32,
+                                  _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "pa_decode_no_alloc": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP]),
     "pa_prefill_varlen": (_I32, [_DESC, _VP, _VP, _I32, _I32, _I64, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _VP, _VP]),
     "pa_validate_metadata": (_I32, [_DESC, _I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP]),
@@ -181,6 +183,18 @@ def pa_decode(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq,
         ctypes.byref(desc), _ptr(q), batch, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_pages_per_seq,
         _ptr(context_lens), max_context_len, scale, max_ctas, _ptr(out), _ptr(workspace), workspace_bytes,
         _stream(stream)))
+
+
+def pa_decode_kv_write(desc, q, k_new, k_row_stride, v_new, v_row_stride, batch, k_cache, v_cache, block_tables,
+                       max_pages_per_seq, context_lens, max_context_len, scale, max_ctas, slot_mapping, out, workspace,
+                       workspace_bytes=None, stream=None):
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("pa_decode_kv_write", lib.pa_decode_kv_write(
+        ctypes.byref(desc), _ptr(q), _ptr(k_new), k_row_stride, _ptr(v_new), v_row_stride, batch, _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), max_pages_per_seq, _ptr(context_lens), max_context_len, scale, max_ctas,
+        _ptr(slot_mapping), _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def pa_decode_no_alloc(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens,

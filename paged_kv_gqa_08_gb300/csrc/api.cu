@@ -276,6 +276,59 @@ pa_status pa_decode(const pa_cache_desc* desc, const void* q, int32_t batch, con
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, const void* k_new, int64_t k_row_stride,
+                             const void* v_new, int64_t v_row_stride, int32_t batch, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
+                             int32_t max_context_len, float scale, int32_t max_ctas, int64_t* slot_mapping,
+                             void* out, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (batch < 0 || max_ctas < 0) return PA_ERR_SHAPE;
+  if (batch == 0) return PA_OK;
+  if (max_pages_per_seq < 1 || max_context_len < 1) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * desc->page_size)
+    return PA_ERR_SHAPE;
+  if (!isfinite(scale)) return PA_ERR_SHAPE;
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  const int64_t re = row_elems(desc);
+  if (k_row_stride < re || v_row_stride < re) return PA_ERR_SHAPE;
+  if (!stride_ok(desc, k_row_stride, re) || !stride_ok(desc, v_row_stride, re)) return PA_ERR_ALIGN;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(out))
+    return PA_ERR_ALIGN;
+  if (desc->num_pages * desc->page_size >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+  if (!workspace) return PA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGN;
+  unsigned int* err = nullptr;
+  if ((st = prepare(&err)) != PA_OK) return st;
+  DecodePlan pl;
+  cudaError_t e = plan_decode(*desc, batch, max_context_len, max_ctas, &pl);
+  if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (workspace_bytes < pl.ws_bytes) return PA_ERR_WORKSPACE;
+  DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.workspace = workspace;
+  a.err = err;
+  a.batch = batch;
+  a.max_pages = max_pages_per_seq;
+  a.max_context_len = max_context_len;
+  a.scale = scale;
+  const int E = elem_bytes(desc->dtype);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_new_stride_bytes = k_row_stride * E;
+  a.v_new_stride_bytes = v_row_stride * E;
+  a.slot_out = slot_mapping;
+  e = launch_decode(*desc, pl, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
                             int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,

@@ -72,6 +72,13 @@ struct KParams {
   uint32_t off_bar, off_meta, off_p, off_alpha, off_ml, off_abort;
   int32_t p_row;        // floats per token row of the probability tile
   float scale_log2;     // softmax scale * log2(e)
+  // Fused KV write (k_new != nullptr): the new token of request b is row b of
+  // k_new / v_new; it is attended from there and stored into its cache slot
+  // (position context_lens[b] - 1) by the CTA that owns the request's last chunk.
+  const char* k_new;
+  const char* v_new;
+  int64_t k_new_stride, v_new_stride;  // bytes
+  int64_t* slot_out;                   // optional: the slot written for request b
 };
 
 // ---------------------------------------------------------------------------
@@ -94,6 +101,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
         cnt = (L + T - 1) >> p.log2T;
       } else {
         raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
+        if (p.k_new != nullptr && p.slot_out) p.slot_out[b] = -1;
       }
     }
     int x = cnt;
@@ -249,7 +257,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
     for (int xg = x0; xg < x1 && !aborted; xg += 32) {
       const int nvalid = min(32, x1 - xg);
       const int x = xg + lane;
-      int my_b = b, n = 0, flags = 0;
+      int my_b = b, n = 0, flags = 0, new_slot = -1;
       long long off = 0;
       if (lane < nvalid) {
         while (my_b < p.B - 1 && p.cs[my_b + 1] <= x) ++my_b;
@@ -265,7 +273,9 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
           off = ((static_cast<long long>(page) << p.log2P) + (t0 & (p.P - 1))) * p.row_bytes;
         }
         flags = ((x == x0 || jc == 0) ? 1 : 0) | ((x == x1 - 1 || x == cb1 - 1) ? 2 : 0) |
-                ((cb0 >= x0 && cb1 <= x1) ? 4 : 0);
+                ((cb0 >= x0 && cb1 <= x1) ? 4 : 0) | ((x == cb1 - 1) ? 8 : 0);
+        if (p.k_new != nullptr && (flags & 8) && n >= 1)
+          new_slot = static_cast<int>(off / p.row_bytes) + n - 1;  // position context_len - 1
       }
       b = __shfl_sync(0xffffffffu, my_b, nvalid - 1);
       for (int u = 0; u < nvalid; ++u) {
@@ -273,6 +283,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
         const int un = __shfl_sync(0xffffffffu, n, u);
         const int uf = __shfl_sync(0xffffffffu, flags, u);
         const long long uoff = __shfl_sync(0xffffffffu, off, u);
+        const int uslot = __shfl_sync(0xffffffffu, new_slot, u);
         int ok = 1;
         if (lane == 0) {
           const int it = xg - x0 + u;
@@ -280,14 +291,25 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
           if (!mbar_wait_bounded(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag, p.err)) {
             ok = 0;
           } else {
-            meta[s] = make_int4(ub, un, uf, 0);
+            meta[s] = make_int4(ub, un, uf, uslot);
             const uint32_t bytes = static_cast<uint32_t>(un) * static_cast<uint32_t>(p.row_bytes);
             mbar_arrive_expect_tx(&full[s], 2 * bytes);
-            if (bytes) {
-              unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
+            unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
+            if (uslot >= 0) {
+              // the cached rows of the chunk, then the new token's row from k_new / v_new
+              const uint32_t cached = bytes - p.row_bytes;
+              if (cached) {
+                bulk_g2s_hint(dst, p.k_cache + uoff, cached, &full[s], pol);
+                bulk_g2s_hint(dst + p.chunk_bytes, p.v_cache + uoff, cached, &full[s], pol);
+              }
+              bulk_g2s(dst + cached, p.k_new + ub * p.k_new_stride, p.row_bytes, &full[s]);
+              bulk_g2s(dst + p.chunk_bytes + cached, p.v_new + ub * p.v_new_stride, p.row_bytes, &full[s]);
+              if (p.slot_out) p.slot_out[ub] = uslot;
+            } else if (bytes) {
               bulk_g2s_hint(dst, p.k_cache + uoff, bytes, &full[s], pol);
               bulk_g2s_hint(dst + p.chunk_bytes, p.v_cache + uoff, bytes, &full[s], pol);
             }
+            if (p.k_new != nullptr && (uf & 8) && uslot < 0 && p.slot_out) p.slot_out[ub] = -1;
             ++issued;
           }
         }
@@ -346,6 +368,17 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
 
     const unsigned char* kbuf = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes + h * Gm::RB + j * 16;
     const unsigned char* vbuf = kbuf + p.chunk_bytes;
+    if (md.w >= 0) {
+      // fused KV write: this head's 16-byte pieces of the new row go to its slot
+      // (row slots of the warp take K and V in turn)
+      const int64_t dst_off = static_cast<int64_t>(md.w) * p.row_bytes + h * Gm::RB + j * 16;
+      const int src_off = (n - 1) * p.row_bytes;
+      for (int part = rs; part < 2; part += RPI) {
+        const unsigned char* src = (part == 0 ? kbuf : vbuf) + src_off;
+        char* dst = const_cast<char*>(part == 0 ? p.k_cache : p.v_cache) + dst_off;
+        stg16(dst, *reinterpret_cast<const uint4*>(src));
+      }
+    }
 
     // scores: partial dot products over this lane's 16 bytes of each row
     float a[VP];
@@ -718,6 +751,11 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   p.off_abort = pl.off_abort;
   p.p_row = pl.p_row;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.k_new = static_cast<const char*>(a.k_new);
+  p.v_new = static_cast<const char*>(a.v_new);
+  p.k_new_stride = a.k_new_stride_bytes;
+  p.v_new_stride = a.v_new_stride_bytes;
+  p.slot_out = a.slot_out;
 
   decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   void* args[] = {&p};

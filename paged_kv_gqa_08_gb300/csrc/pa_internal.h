@@ -108,6 +108,11 @@ struct DecodeArgs {
   unsigned int* err;
   int32_t batch, max_pages, max_context_len;
   float scale;
+  // fused KV write of the step's new tokens (all null for plain decode)
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  int64_t k_new_stride_bytes = 0, v_new_stride_bytes = 0;
+  int64_t* slot_out = nullptr;
 };
 cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& plan, const DecodeArgs& a,
                           cudaStream_t s);

@@ -1,0 +1,84 @@
+"""pa_decode_kv_write: the step's KV write fused into decode.  The cache must
+equal the oracle's bit for bit (new rows included), the reported slots must be
+the oracle's slot mapping, and the outputs must match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_harness import GpuRun, as_f64, storage
+from paged_kv_gqa_08_gb300 import PA_DEVERR_BAD_LENGTH, pa_decode_kv_write, pa_read_device_errors
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
+
+
+def _bits(a):
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+def _fused(run, wl, max_ctas=0, ctx=None):
+    t = run.t
+    row = wl.num_kv_heads * wl.head_dim
+    slots = torch.full((wl.batch,), -7, dtype=torch.int64, device="cuda")
+    out = torch.full_like(run.bufs.out, float("nan"))
+    pa_decode_kv_write(run.desc, t["q"], t["k_new"], row, t["v_new"], row, wl.batch, run.k_cache, run.v_cache,
+                       t["block_tables"], wl.max_pages_per_seq, t["context_lens"] if ctx is None else ctx,
+                       wl.max_context_len, wl.scale, max_ctas, slots, out, run.bufs.workspace)
+    torch.cuda.synchronize()
+    return out, slots
+
+
+def _check_all(run, wl, out, slots):
+    ref = oracle.reference_step(wl)
+    ok, err, bound = oracle.within_tolerance(as_f64(out[: wl.batch]), ref["o"], wl.dtype)
+    assert ok, (err, bound)
+    assert np.array_equal(slots.cpu().numpy(), ref["slots"])
+    assert np.array_equal(_bits(storage(run.k_cache)), _bits(ref["k_cache"]))
+    assert np.array_equal(_bits(storage(run.v_cache)), _bits(ref["v_cache"]))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32_decode", "qwen3_0p6b_decode", "qwen3_8b_decode", "long_context_decode"])
+def test_fused_decode_configs(name):
+    wl = synth.make_workload(name)
+    run = GpuRun(wl)                        # cache holds the history only
+    pa_read_device_errors(reset=True)
+    out, slots = _fused(run, wl)
+    _check_all(run, wl, out, slots)
+    assert pa_read_device_errors(reset=True) == 0
+
+
+SMALL = [
+    ("f32", 4, 2, 64, 16, [1, 15, 16, 17, 100]),
+    ("bf16", 24, 8, 128, 16, [1, 2, 77, 500]),
+    ("bf16", 32, 4, 128, 256, [255, 256, 257, 3000]),
+    ("bf16", 4, 4, 64, 16, [9, 200, 31]),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"{c[0]}-hq{c[1]}-hkv{c[2]}-d{c[3]}-p{c[4]}" for c in SMALL])
+@pytest.mark.parametrize("max_ctas", [0, 1, 3])
+def test_fused_decode_small_shapes(case, max_ctas):
+    dtype, Hq, Hkv, hd, P, lens = case
+    wl = synth.make_workload(dict(kind="decode", dtype=dtype, B=len(lens), Hq=Hq, Hkv=Hkv, hd=hd, P=P,
+                                  context_lens=lens, seed=sum(lens) + 5))
+    run = GpuRun(wl, max_ctas=max_ctas)
+    out, slots = _fused(run, wl, max_ctas)
+    _check_all(run, wl, out, slots)
+
+
+def test_fused_decode_reports_skipped_requests():
+    wl = synth.make_workload("qwen3_0p6b_decode", B=6)
+    run = GpuRun(wl)
+    pa_read_device_errors(reset=True)
+    ctx = run.t["context_lens"].clone()
+    ctx[3] = 0
+    out, slots = _fused(run, wl, ctx=ctx)
+    assert pa_read_device_errors(reset=True) & PA_DEVERR_BAD_LENGTH
+    s = slots.cpu().numpy()
+    ref = oracle.reference_step(wl)
+    assert s[3] == -1
+    good = [0, 1, 2, 4, 5]
+    assert np.array_equal(s[good], ref["slots"][good])
+    ok, err, bound = oracle.within_tolerance(as_f64(out[good]), ref["o"][good], wl.dtype)
+    assert ok, (err, bound)
