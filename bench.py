@@ -236,7 +236,8 @@ class Device:
                    torch.empty(nh, dtype=torch.int64, device=dev), self.k_cache, self.v_cache)
         self.t["hist_k"] = self.t["hist_v"] = None
         self.bufs = alloc_step_buffers(self.desc, wl.kind, wl.num_new_tokens, wl.batch, wl.max_context_len, dev,
-                                       norm=wl.q_norm_w is not None, max_ctas=max_ctas)
+                                       norm=wl.q_norm_w is not None, max_ctas=max_ctas,
+                                       max_seqlen_q=max(wl.max_new_len, 1))
         torch.cuda.synchronize()
 
     def write_part(self):
@@ -272,7 +273,7 @@ class Device:
         else:
             pa_prefill_varlen(self.desc, q, t["cu_seqlens_q"], wl.batch, wl.max_new_len, wl.num_new_tokens,
                               self.k_cache, self.v_cache, t["block_tables"], wl.max_pages_per_seq,
-                              t["context_lens"], wl.max_context_len, wl.scale, b.out)
+                              t["context_lens"], wl.max_context_len, wl.scale, b.out, b.workspace)
 
 
 def barrier(world):

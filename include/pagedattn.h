@@ -267,12 +267,39 @@ PA_API pa_status pa_decode_no_alloc(const pa_cache_desc* desc, const void* q, in
  *   out              [num_tokens, num_q_heads, head_dim] contiguous.
  * bf16 with head_dim 128 runs on the tcgen05 tensor cores; other cases on a
  * CUDA-core kernel.
+ *   workspace        optional device buffer (256-byte aligned) of
+ *                    workspace_bytes >= pa_prefill_workspace_size(...), used
+ *                    only by the tensor-core path; owned by the caller, not
+ *                    read by the host, contents need not be initialised.  With
+ *                    it, a planner kernel splits long key ranges over several
+ *                    CTAs and orders the work longest first, and a merge
+ *                    kernel combines the parts by their log-sum-exp (the
+ *                    decode split-KV rule); without it
+ *                    (NULL) each CTA takes one pair of 128-row q-tiles with
+ *                    all its keys.  Results
+ *                    agree within the bf16 tolerance either way; a too small
+ *                    workspace returns PA_ERR_WORKSPACE.  Calls sharing one
+ *                    workspace must be ordered on the GPU (same stream).
+ *                    Once a planned call has run, the workspace's first 16
+ *                    bytes hold int32 {CTAs per kv-head, split pairs, part
+ *                    size in 128-key tiles, q-tile pairs} (diagnostics).
  */
 PA_API pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q,
-                            int32_t batch, int32_t max_seqlen_q, int64_t num_tokens,
-                            const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                            int32_t max_pages_per_seq, const int32_t* context_lens,
-                            int32_t max_context_len, float scale, void* out, pa_stream_t stream);
+                                   int32_t batch, int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables, int32_t max_pages_per_seq,
+                                   const int32_t* context_lens, int32_t max_context_len, float scale, void* out,
+                                   void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_prefill_workspace_size -- bytes of the optional pa_prefill_varlen
+ * workspace for these bounds on the current device (it holds the work list
+ * and, for split ranges, fp32 partial outputs of at most 4 waves of CTAs:
+ * about 80 MiB on a 152-SM GPU), or 0 when the call would not use one
+ * (fp32 or head_dim 64, max_context_len beyond 65535 * 128) or the
+ * arguments are invalid.
+ */
+PA_API size_t pa_prefill_workspace_size(const pa_cache_desc* desc, int32_t batch, int32_t max_seqlen_q,
+                                        int64_t num_tokens, int32_t max_context_len);
 
 /*
  * pa_validate_metadata -- opt-in device check of the metadata the other calls

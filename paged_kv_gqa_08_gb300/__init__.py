@@ -83,7 +83,9 @@ _SIGS = {
     "pa_decode_kv_write": (_I32, [_DESC, _VP, _VP, _I64, _VP, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32,
                                   _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "pa_decode_no_alloc": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP]),
-    "pa_prefill_varlen": (_I32, [_DESC, _VP, _VP, _I32, _I32, _I64, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _VP, _VP]),
+    "pa_prefill_varlen": (_I32, [_DESC, _VP, _VP, _I32, _I32, _I64, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _VP, _VP,
+                                 ctypes.c_size_t, _VP]),
+    "pa_prefill_workspace_size": (ctypes.c_size_t, [_DESC, _I32, _I32, _I64, _I32]),
     "pa_validate_metadata": (_I32, [_DESC, _I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP]),
     "pa_selftest_bounded_wait": (_I32, [_I32, _VP]),
     "pa_read_device_errors": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32]),
@@ -207,12 +209,20 @@ def pa_decode_no_alloc(desc, q, batch, k_cache, v_cache, block_tables, max_pages
 
 
 def pa_prefill_varlen(desc, q, cu_seqlens_q, batch, max_seqlen_q, num_tokens, k_cache, v_cache, block_tables,
-                      max_pages_per_seq, context_lens, max_context_len, scale, out, stream=None):
+                      max_pages_per_seq, context_lens, max_context_len, scale, out, workspace=None,
+                      workspace_bytes=None, stream=None):
     lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("pa_prefill_varlen", lib.pa_prefill_varlen(
         ctypes.byref(desc), _ptr(q), _ptr(cu_seqlens_q), batch, max_seqlen_q, num_tokens, _ptr(k_cache),
         _ptr(v_cache), _ptr(block_tables), max_pages_per_seq, _ptr(context_lens), max_context_len, scale,
-        _ptr(out), _stream(stream)))
+        _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def pa_prefill_workspace_size(desc, batch, max_seqlen_q, num_tokens, max_context_len) -> int:
+    return int(load_library().pa_prefill_workspace_size(ctypes.byref(desc), batch, max_seqlen_q, num_tokens,
+                                                        max_context_len))
 
 
 def pa_validate_metadata(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq,

@@ -332,7 +332,8 @@ pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, const voi
 pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
                             int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
-                            int32_t max_context_len, float scale, void* out, pa_stream_t stream) {
+                            int32_t max_context_len, float scale, void* out, void* workspace,
+                            size_t workspace_bytes, pa_stream_t stream) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
   if (batch < 0 || num_tokens < 0 || max_seqlen_q < 0) return PA_ERR_SHAPE;
@@ -344,6 +345,15 @@ pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int3
   if (!isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
   if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
+  cudaError_t e;
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGN;
+    PrefillPlan plan;
+    if ((e = plan_prefill(*desc, batch, max_seqlen_q, num_tokens, max_context_len, &plan)) != cudaSuccess)
+      return cuda_fail(e);
+    if (plan.ws_bytes == 0) workspace = nullptr;  // this call is never planned
+    else if (workspace_bytes < plan.ws_bytes) return PA_ERR_WORKSPACE;
+  }
   unsigned int* err = nullptr;
   if ((st = prepare(&err)) != PA_OK) return st;
   PrefillArgs a{};
@@ -361,12 +371,23 @@ pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int3
   a.max_pages = max_pages_per_seq;
   a.max_context_len = max_context_len;
   a.scale = scale;
-  cudaError_t e;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   if (desc->dtype == PA_BF16 && desc->head_dim == 128)
     e = launch_prefill_tc(*desc, a, static_cast<cudaStream_t>(stream));
   else
     e = launch_prefill_simt(*desc, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t pa_prefill_workspace_size(const pa_cache_desc* desc, int32_t batch, int32_t max_seqlen_q,
+                                 int64_t num_tokens, int32_t max_context_len) {
+  if (check_desc(desc) != PA_OK || batch < 1 || max_seqlen_q < 1 || num_tokens < 1 || max_context_len < 1 ||
+      max_seqlen_q > max_context_len || num_tokens > 0x7fffffff)
+    return 0;
+  PrefillPlan plan;
+  if (plan_prefill(*desc, batch, max_seqlen_q, num_tokens, max_context_len, &plan) != cudaSuccess) return 0;
+  return plan.ws_bytes;
 }
 
 pa_status pa_validate_metadata(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,

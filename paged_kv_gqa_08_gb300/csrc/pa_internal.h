@@ -132,7 +132,19 @@ struct PrefillArgs {
   int64_t num_tokens;
   int32_t batch, max_seqlen_q, max_pages, max_context_len;
   float scale;
+  // Caller workspace for the planned tensor-core launch (null: one CTA per
+  // q-tile pair in grid order, no split).
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
 };
+// Workspace layout of the planned tensor-core prefill (byte offsets, each
+// 256-aligned); ws_bytes == 0 when the call cannot be planned.
+struct PrefillPlan {
+  int32_t pair_cap, slot_cap, unit_cap, split_cap, n_sm;
+  size_t off_hdr, off_pairs, off_units, off_splits, off_lse, off_o, ws_bytes;
+};
+cudaError_t plan_prefill(const pa_cache_desc& d, int32_t batch, int32_t max_seqlen_q, int64_t num_tokens,
+                         int32_t max_context_len, PrefillPlan* out);
 // CUDA-core kernel (any supported dtype / head_dim).
 cudaError_t launch_prefill_simt(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s);
 // tcgen05 tensor-core kernel (bf16, head_dim 128).

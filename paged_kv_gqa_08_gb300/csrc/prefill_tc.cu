@@ -29,10 +29,18 @@
 //       O_0 256-383, O_1 384-511.
 // Every wait is bounded; a timeout raises PA_DEVERR_TIMEOUT and the CTA
 // drains its copies and MMAs, frees its TMEM and returns.
+//
+// Planned launch (the caller gives a workspace): a one-CTA planner kernel
+// turns the pairs into units, cutting long key ranges into parts and listing
+// the units longest first; a CTA then runs one (unit, kv-head), a part writes
+// O / l and the row log-sum-exp in fp32, and a merge kernel combines the
+// parts of each split pair (flash-decoding's split-KV rule, applied to
+// prefill rows).
 #include <cuda.h>
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -70,9 +78,18 @@ struct TcParams {
   const int32_t* ctx;
   char* out;
   unsigned int* err;
-  int64_t num_pages;
+  int64_t num_pages, num_tokens;
   int32_t B, Hq, Hkv, G, TQ, P, log2P, maxp, max_ctx;
   float scale_log2;
+  // Planned launch (all null without a workspace): CTA x of the 1-D grid runs
+  // kv-head x % Hkv of unit x / Hkv, units[u] = {request, q-tile pair,
+  // first key tile | (end key tile << 16), partial slot or -1}.  A unit with a
+  // slot covers part of its pair's keys and writes O / l and the base-2
+  // log-sum-exp of each row to o_part / lse_part for the merge kernel.
+  const int4* units;
+  const int32_t* n_units;
+  float* o_part;    // [slot][Hkv][2 q-tiles][128 rows][128]
+  float* lse_part;  // [slot][Hkv][2 q-tiles][128 rows]
 };
 
 // ---------------------------------------------------------------------------
@@ -213,14 +230,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-  const int qp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int h, b, qp, j_lo = 0, j_hi = 1 << 30, slot = -1;
+  if (p.units) {
+    const int u = static_cast<int>(blockIdx.x) / p.Hkv;
+    h = static_cast<int>(blockIdx.x) - u * p.Hkv;
+    if (u >= *p.n_units) return;
+    const int4 ud = p.units[u];
+    b = ud.x;
+    qp = ud.y;
+    j_lo = ud.z & 0xffff;
+    j_hi = static_cast<int>(static_cast<uint32_t>(ud.z) >> 16);
+    slot = ud.w;
+  } else {
+    h = blockIdx.y;
+    b = blockIdx.z;
+    qp = blockIdx.x;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s0 = p.cu[b], s1 = p.cu[b + 1];
   const int n = s1 - s0;
   if (2 * qp * p.TQ >= n) return;
   const int L = p.ctx[b];
   const int cap = min(p.max_ctx, p.maxp << p.log2P);
-  if (s0 < 0 || L < n || L > cap) {
+  if (s0 < 0 || s1 > p.num_tokens || L < n || L > cap) {
     if (threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
     return;
   }
@@ -233,8 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     pos0[g] = L - n + qt * p.TQ;                       // position of its first token
     ntg[g] = g < nq ? (pos0[g] + rows[g] + kBN - 1) / kBN : 0;  // key tiles it needs
   }
+  // This unit's key tiles: [j_lo, j_hi) of the pair's [0, ntg).  ntl[g] is the
+  // number q-tile g processes; local tile index jl = j - j_lo.
   const int kv_len = pos0[nq - 1] + rows[nq - 1];
-  const int nt = ntg[nq - 1];
+  j_hi = min(j_hi, ntg[nq - 1]);
+  const int nt = j_hi - j_lo;
+  if (nt <= 0) return;
+  int ntl[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) ntl[g] = max(0, min(j_hi, ntg[g]) - j_lo);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars + 0;
@@ -302,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int j = 0; j < nt && ok; ++j) {
       const int st = j & 1;
       const uint32_t par = ((j >> 1) & 1) ^ 1;
-      const int t0 = j * kBN;
+      const int t0 = (j_lo + j) * kBN;
       const int valid = min(kBN, kv_len - t0);
       const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
       int y_full = -1, y_rem = -1;
@@ -388,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (ok) ok = mbar_wait_bounded(&k_full[0], 0, abort_flag, p.err);
       if (ok) {
         tc_fence_after();
-        for (int g = 0; g < nq; ++g) qk(g, 0);
+        for (int g = 0; g < nq; ++g)
+          if (ntl[g] > 0) qk(g, 0);
         mma_commit(&k_empty[0]);
       }
       for (int j = 0; j < nt && ok; ++j) {
@@ -396,15 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (!(ok = mbar_wait_bounded(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.err))) break;
         // q-tile 0: PV of tile j, then QK of tile j+1 (the tensor pipe runs them
         // in issue order, so QK overwrites S_0 only after PV has read P_0)
-        if (j < ntg[0] && !(ok = pv(0, j))) break;
+        if (j < ntl[0] && !(ok = pv(0, j))) break;
         if (more) {
           if (!(ok = mbar_wait_bounded(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.err))) break;
           tc_fence_after();
-          if (j + 1 < ntg[0]) qk(0, j + 1);
+          if (j + 1 < ntl[0]) qk(0, j + 1);
         }
         // q-tile 1
-        if (j < ntg[1] && !(ok = pv(1, j))) break;
-        if (more && j + 1 < ntg[1]) qk(1, j + 1);
+        if (j < ntl[1] && !(ok = pv(1, j))) break;
+        if (more && j + 1 < ntl[1]) qk(1, j + 1);
         mma_commit(&v_empty[j & 1]);
         if (more) mma_commit(&k_empty[(j + 1) & 1]);
       }
@@ -423,14 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int pos_r = pos0[g] + t;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntg[g]; ++j) {
+    for (int j = 0; j < ntl[g]; ++j) {
       ok = mbar_wait_bounded(&s_full[g], j & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int key0 = j * kBN;
+      const int key0 = (j_lo + j) * kBN;
       const bool need_mask = key0 + kBN - 1 > pos0[g];
       // One TMEM round trip per tile: all 128 scores of the row are loaded
       // (four loads, one wait), the row max is taken over the raw scores (the
@@ -506,8 +546,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[g]);
     }
-    // epilogue: O / l to global memory
-    if (g < nq) {
+    // epilogue: O / l to global memory, or this part's partial result
+    if (g < nq && slot >= 0) {
+      if (ok) ok = mbar_wait_bounded(o_final, 0, abort_flag, p.err);
+      const int64_t prow = ((static_cast<int64_t>(slot) * p.Hkv + h) * 2 + g) * kBM + row;
+      if (__all_sync(0xffffffffu, ok)) {
+        if (ntl[g] > 0) {
+          tc_fence_after();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          float* dstp = p.o_part + prow * 128;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + colO + 32 * c, o);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              *reinterpret_cast<float4*>(dstp + 32 * c + 4 * q4) =
+                  make_float4(__uint_as_float(o[4 * q4]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
+                              __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+          }
+          p.lse_part[prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
+        } else {
+          p.lse_part[prow] = -INFINITY;  // no key tile of this part reaches q-tile g
+        }
+      }
+    } else if (g < nq) {
       if (ok) ok = mbar_wait_bounded(o_final, 0, abort_flag, p.err);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
@@ -542,6 +605,307 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
+// planner: q-tile pairs -> units (split long key ranges, longest first)
+// ---------------------------------------------------------------------------
+// A CTA of the attention kernel runs one unit.  Without a plan the units are
+// the q-tile pairs themselves in grid order, so a batch whose pairs fill less
+// than a wave, or whose last wave holds its longest pairs, waits on its
+// longest pair.  The planner (one CTA, on the device, so the launch needs no
+// host copy of the lengths and can be captured in a graph) lists the pairs
+// with their key-tile counts nt, chooses a part size tau, cuts every pair
+// with nt > tau into ceil(nt / tau) near-equal key ranges, and writes the
+// units sorted by length, longest first, so that the hardware block
+// scheduler, which starts CTAs in index order as SMs free up, approximates
+// longest-processing-time-first list scheduling.
+//
+// tau minimises an estimate of the makespan in units of one key tile of one
+// CTA: a unit costs its length + 1 (prologue, epilogue) + 1 more when it is a
+// part (partial store, merge); with U CTAs of largest cost c_max and mean
+// load A = total cost / SMs, the estimate is min(ceil(U / SMs) * c_max,
+// A + c_max) (the waves bound and the list-scheduling bound).  Splitting is
+// considered only while the pairs fill at most four waves; beyond that the
+// ordering alone keeps the tail short.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 2048;   // unit lengths >= 2047 tiles share the last bucket
+constexpr int kPlanSmemPairs = 2048; // pairs kept in shared memory (the rest are re-read from the workspace)
+constexpr int kPlanCandidates = 32;  // one per warp
+constexpr int kSplitWaves = 4;
+constexpr int kMaxSlots = 65535;     // slot counts are scanned in 16 bits
+
+struct PlanParams {
+  const int32_t* cu;
+  const int32_t* ctx;
+  unsigned int* err;
+  int4* pairs;   // [pair_cap] {request, pair, nt, 0}
+  int4* units;   // [pair_cap + slot_cap]
+  int4* splits;  // [split_cap] {request, pair, first slot, parts}
+  int32_t* hdr;  // {units, split pairs, tau, pairs}
+  int64_t num_tokens;
+  int32_t B, TQ, Hkv, n_sm, max_seqlen_q, cap_ctx, pair_cap, slot_cap, split_cap;
+};
+
+// Exclusive prefix sum over the CTA (blockDim.x a multiple of 32, <= 1024).
+template <typename T>
+PA_DEVINL T block_scan_excl(T v, T* sh, T* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < nw ? sh[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sh[lane] = w;
+  }
+  __syncthreads();
+  const T r = (warp > 0 ? sh[warp - 1] : T(0)) + x - v;
+  *total = sh[nw - 1];
+  __syncthreads();
+  return r;
+}
+
+PA_DEVINL int parts_of(int nt, int tau) { return (nt + tau - 1) / tau; }
+
+// A pair of nt key tiles cut into `parts` ranges: the first nt % parts ranges
+// hold one tile more than the others (lengths base + 1 and base).
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanParams q) {
+  __shared__ unsigned long long sh_scan[32];
+  __shared__ int cursor[kPlanBuckets];
+  __shared__ int4 sh_pairs[kPlanSmemPairs];
+  __shared__ float cand_est[kPlanCandidates];
+  __shared__ int cand_tau[kPlanCandidates];
+  __shared__ int sh_max_nt, sh_tau;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) sh_max_nt = 0;
+  for (int i = tid; i < kPlanBuckets; i += kPlanThreads) cursor[i] = 0;
+
+  // 1. the q-tile pairs of every request and their key-tile counts
+  unsigned long long carry = 0;
+  int max_nt = 0;
+  for (int base = 0; base < q.B; base += kPlanThreads) {
+    const int b = base + tid;
+    int np = 0, n = 0, L = 0;
+    if (b < q.B) {
+      const int s0 = q.cu[b], s1 = q.cu[b + 1];
+      n = s1 - s0;
+      L = q.ctx[b];
+      if (s0 < 0 || n < 0 || s1 > q.num_tokens || n > q.max_seqlen_q || L < n || L > q.cap_ctx)
+        raise_flag(q.err, PA_DEVERR_BAD_LENGTH);
+      else
+        np = ((n + q.TQ - 1) / q.TQ + 1) / 2;
+    }
+    unsigned long long tot;
+    const unsigned long long off = carry + block_scan_excl<unsigned long long>(np, sh_scan, &tot);
+    for (int k = 0; k < np; ++k) {
+      const int nt = (L - n + min((2 * k + 2) * q.TQ, n) + kBN - 1) / kBN;
+      const int4 pr = make_int4(b, k, nt, 0);
+      if (off + k < static_cast<unsigned long long>(q.pair_cap)) q.pairs[off + k] = pr;
+      if (off + k < kPlanSmemPairs) sh_pairs[off + k] = pr;
+      max_nt = max(max_nt, nt);
+    }
+    carry += tot;
+  }
+  if (max_nt > 0) atomicMax(&sh_max_nt, max_nt);
+  if (carry > static_cast<unsigned long long>(q.pair_cap)) {  // lengths disagree with the workspace's sizes
+    if (tid == 0) {
+      raise_flag(q.err, PA_DEVERR_BAD_LENGTH);
+      q.hdr[0] = q.hdr[1] = q.hdr[2] = q.hdr[3] = 0;
+    }
+    return;
+  }
+  const int n_pairs = static_cast<int>(carry);
+  __syncthreads();
+  max_nt = sh_max_nt;
+  auto pair_at = [&](int i) -> int4 { return i < kPlanSmemPairs ? sh_pairs[i] : q.pairs[i]; };
+
+  // 2. the part size: one candidate per warp, from max_nt (no split) down to 2
+  int tau = max(max_nt, 1);
+  if (n_pairs > 0 && max_nt > 2 &&
+      static_cast<int64_t>(n_pairs) * q.Hkv <= static_cast<int64_t>(kSplitWaves) * q.n_sm) {
+    const int n_cand = min(kPlanCandidates, max_nt - 1);
+    if (warp < n_cand) {
+      const int c = warp;
+      const int t_c = max_nt <= kPlanCandidates
+                          ? max_nt - c
+                          : max(2, static_cast<int>(ceilf(max_nt * exp2f(-log2f(0.5f * max_nt) * c / (n_cand - 1)))));
+      int units = 0, slots = 0, work = 0, cmax = 0;
+      for (int i = lane; i < n_pairs; i += 32) {
+        const int nt = pair_at(i).z;
+        const int parts = parts_of(nt, t_c);
+        const int split = parts > 1;
+        units += parts;
+        slots += split ? parts : 0;
+        work += nt + parts * (1 + split);
+        cmax = max(cmax, (nt + parts - 1) / parts + 1 + split);
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        units += __shfl_xor_sync(0xffffffffu, units, o);
+        slots += __shfl_xor_sync(0xffffffffu, slots, o);
+        work += __shfl_xor_sync(0xffffffffu, work, o);
+        cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      }
+      if (lane == 0) {
+        const float ctas = static_cast<float>(units) * q.Hkv;
+        const float waves = ceilf(ctas / q.n_sm);
+        const float mean = static_cast<float>(work) * q.Hkv / q.n_sm;
+        cand_est[c] = slots > q.slot_cap ? INFINITY : fminf(waves * cmax, mean + cmax);
+        cand_tau[c] = t_c;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // arg-min; ties go to the lower index (the larger part size)
+      float e = lane < n_cand ? cand_est[lane] : INFINITY;
+      int c = lane;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float e2 = __shfl_xor_sync(0xffffffffu, e, o);
+        const int c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        if (e2 < e || (e2 == e && c2 < c)) {
+          e = e2;
+          c = c2;
+        }
+      }
+      if (lane == 0) sh_tau = e < INFINITY ? cand_tau[c] : max_nt;  // candidate 0 (no split) is always finite
+    }
+    __syncthreads();
+    tau = sh_tau;
+  }
+
+  // 3. histogram of unit lengths, then bucket cursors in descending length order
+  for (int i = tid; i < n_pairs; i += kPlanThreads) {
+    const int nt = pair_at(i).z;
+    const int parts = parts_of(nt, tau), base = nt / parts, rem = nt - base * parts;
+    if (rem) atomicAdd(&cursor[min(base + 1, kPlanBuckets - 1)], rem);
+    if (parts > rem) atomicAdd(&cursor[min(base, kPlanBuckets - 1)], parts - rem);
+  }
+  __syncthreads();
+  {
+    static_assert(kPlanBuckets == 2 * kPlanThreads, "two buckets per thread");
+    const int hi = kPlanBuckets - 1 - 2 * tid, lo = hi - 1;
+    const int c_hi = cursor[hi], c_lo = cursor[lo];
+    unsigned long long tot;
+    const int ex = static_cast<int>(block_scan_excl<unsigned long long>(c_hi + c_lo, sh_scan, &tot));
+    cursor[hi] = ex;
+    cursor[lo] = ex + c_hi;
+    __syncthreads();
+  }
+
+  // 4. units, partial slots and the split list; one scan of
+  //    units (bits 0-31) | slots (32-47) | split pairs (48-63)
+  unsigned long long acc = 0;
+  for (int b0 = 0; b0 < n_pairs; b0 += kPlanThreads) {
+    const int i = b0 + tid;
+    int4 pr = make_int4(0, 0, 0, 0);
+    int parts = 0;
+    if (i < n_pairs) {
+      pr = pair_at(i);
+      parts = parts_of(pr.z, tau);
+    }
+    const int split = parts > 1;
+    const unsigned long long mine = static_cast<unsigned long long>(parts) |
+                                    (static_cast<unsigned long long>(split ? parts : 0) << 32) |
+                                    (static_cast<unsigned long long>(split) << 48);
+    unsigned long long tot;
+    const unsigned long long before = acc + block_scan_excl<unsigned long long>(mine, sh_scan, &tot);
+    if (parts > 0) {
+      const int slot0 = static_cast<int>((before >> 32) & 0xffff), si = static_cast<int>(before >> 48);
+      const int base = pr.z / parts, rem = pr.z - base * parts;
+      const int p_hi = rem ? atomicAdd(&cursor[min(base + 1, kPlanBuckets - 1)], rem) : 0;
+      const int p_lo = parts > rem ? atomicAdd(&cursor[min(base, kPlanBuckets - 1)], parts - rem) : 0;
+      for (int k = 0; k < parts; ++k) {
+        const int j0 = k * base + min(k, rem);
+        const int j1 = j0 + base + (k < rem);
+        const int pos = k < rem ? p_hi + k : p_lo + (k - rem);
+        q.units[pos] = make_int4(pr.x, pr.y, j0 | (j1 << 16), split ? slot0 + k : -1);
+      }
+      if (split) q.splits[si] = make_int4(pr.x, pr.y, slot0, parts);
+    }
+    acc += tot;
+  }
+  if (tid == 0) {
+    q.hdr[0] = static_cast<int>(acc & 0xffffffffu);
+    q.hdr[1] = static_cast<int>(acc >> 48);
+    q.hdr[2] = tau;
+    q.hdr[3] = n_pairs;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// merge of split pairs: O = sum_k 2^(lse_k - M) O_k / sum_k 2^(lse_k - M)
+// ---------------------------------------------------------------------------
+constexpr int kMergeThreads = 256;                     // 8 warps = 8 rows per CTA
+constexpr int kMergeRowBlocks = 2 * kBM / (kMergeThreads / 32);
+
+struct MergeParams {
+  const int32_t* cu;
+  const int4* splits;
+  const int32_t* hdr;
+  const float* o_part;
+  const float* lse_part;
+  char* out;
+  int32_t Hq, Hkv, G, TQ;
+};
+
+// CTA = (8 rows of a split pair, kv-head); a warp per row, 4 dims per lane.
+// The parts' log-sum-exps are loaded one per lane and reduced by shuffles;
+// the O loads of four parts are in flight together.
+__global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const MergeParams m) {
+  const int si = blockIdx.x / kMergeRowBlocks, h = blockIdx.y;
+  if (si >= m.hdr[1]) return;
+  const int4 sp = m.splits[si];
+  const int b = sp.x, qp = sp.y, slot0 = sp.z, parts = sp.w;
+  const int s0 = m.cu[b], n = m.cu[b + 1] - s0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (blockIdx.x % kMergeRowBlocks) * (kMergeThreads / 32) + warp;  // row of the pair, 0..255
+  const int g = r / kBM, row = r % kBM;
+  const int t = row / m.G, gg = row - t * m.G;
+  const int tok = (2 * qp + g) * m.TQ + t;
+  if (tok >= n) return;
+  const int64_t slot_stride = static_cast<int64_t>(m.Hkv) * 2 * kBM;  // rows per slot
+  const int64_t r0 = (static_cast<int64_t>(slot0) * m.Hkv + h) * 2 * kBM + r;
+  float mx = -INFINITY;
+  for (int k = lane; k < parts; k += 32) mx = fmaxf(mx, m.lse_part[r0 + k * slot_stride]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int k0 = 0; k0 < parts; k0 += 32) {
+    const int k = k0 + lane;
+    const float lse = k < parts ? m.lse_part[r0 + k * slot_stride] : -INFINITY;
+    const float w_mine = lse == -INFINITY ? 0.f : exp2f(lse - mx);
+    const int kn = min(32, parts - k0);
+#pragma unroll 4
+    for (int i = 0; i < kn; ++i) {
+      const float w = __shfl_sync(0xffffffffu, w_mine, i);
+      const float4 o =
+          *reinterpret_cast<const float4*>(m.o_part + (r0 + (k0 + i) * slot_stride) * 128 + 4 * lane);
+      if (w != 0.f) {
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+        wsum += w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint2 v;
+  v.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  v.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(m.out + ((static_cast<int64_t>(s0) + tok) * m.Hq + h * m.G + gg) * 256 + 8 * lane) = v;
+}
+
+// ---------------------------------------------------------------------------
 // host side: tensor maps and launch
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -571,6 +935,45 @@ bool encode(EncodeTiledFn fn, CUtensorMap* m, const void* base, int rank, const 
 }
 
 }  // namespace
+
+cudaError_t plan_prefill(const pa_cache_desc& d, int32_t batch, int32_t max_seqlen_q, int64_t num_tokens,
+                         int32_t max_context_len, PrefillPlan* out) {
+  memset(out, 0, sizeof(*out));
+  // Only the tensor-core path is planned; unit descriptors hold key tiles in 16 bits.
+  if (d.dtype != PA_BF16 || d.head_dim != 128) return cudaSuccess;
+  if ((static_cast<int64_t>(max_context_len) + kBN - 1) / kBN > 0xffff) return cudaSuccess;
+  if (batch < 1 || max_seqlen_q < 1 || num_tokens < 1) return cudaSuccess;
+  DeviceInfo di;
+  cudaError_t e = current_device_info(&di);
+  if (e != cudaSuccess) return e;
+  const int G = d.num_q_heads / d.num_kv_heads, TQ = kBM / G;
+  const int64_t pmax = ((max_seqlen_q + TQ - 1) / TQ + 1) / 2;
+  const int64_t pair_cap = std::min<int64_t>(batch * pmax, num_tokens / (2 * TQ) + batch);
+  if (pair_cap > (1 << 30)) return cudaSuccess;
+  PrefillPlan& pl = *out;
+  pl.n_sm = di.sm_count;
+  pl.pair_cap = static_cast<int32_t>(pair_cap);
+  pl.slot_cap = std::min(kMaxSlots, (kSplitWaves * di.sm_count + d.num_kv_heads - 1) / d.num_kv_heads);
+  pl.split_cap = pl.slot_cap / 2;
+  pl.unit_cap = pl.pair_cap + pl.slot_cap;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off = 0;
+  pl.off_hdr = off;
+  off = up(off + 4 * sizeof(int32_t));
+  pl.off_pairs = off;
+  off = up(off + static_cast<size_t>(pl.pair_cap) * sizeof(int4));
+  pl.off_units = off;
+  off = up(off + static_cast<size_t>(pl.unit_cap) * sizeof(int4));
+  pl.off_splits = off;
+  off = up(off + static_cast<size_t>(std::max(pl.split_cap, 1)) * sizeof(int4));
+  const size_t rows = static_cast<size_t>(pl.slot_cap) * d.num_kv_heads * 2 * kBM;
+  pl.off_lse = off;
+  off = up(off + rows * sizeof(float));
+  pl.off_o = off;
+  off = up(off + rows * 128 * sizeof(float));
+  pl.ws_bytes = off;
+  return cudaSuccess;
+}
 
 cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s) {
   if (a.num_tokens == 0 || a.batch == 0) return cudaSuccess;
@@ -605,6 +1008,7 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   p.out = static_cast<char*>(a.out);
   p.err = a.err;
   p.num_pages = d.num_pages;
+  p.num_tokens = a.num_tokens;
   p.B = a.batch;
   p.Hq = d.num_q_heads;
   p.Hkv = d.num_kv_heads;
@@ -631,10 +1035,63 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
       done[dev] = true;
     }
   }
-  const int qtiles = (a.max_seqlen_q + TQ - 1) / TQ;
-  const dim3 grid((qtiles + 1) / 2, d.num_kv_heads, a.batch);
-  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  if (!a.workspace) {
+    const int qtiles = (a.max_seqlen_q + TQ - 1) / TQ;
+    const dim3 grid((qtiles + 1) / 2, d.num_kv_heads, a.batch);
+    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+  }
+
+  // planned launch: planner -> attention units -> merge of split pairs
+  PrefillPlan pl;
+  cudaError_t e = plan_prefill(d, a.batch, a.max_seqlen_q, a.num_tokens, a.max_context_len, &pl);
+  if (e != cudaSuccess) return e;
+  if (pl.ws_bytes == 0 || a.workspace_bytes < pl.ws_bytes) return cudaErrorInvalidValue;
+  char* ws = static_cast<char*>(a.workspace);
+  PlanParams q;
+  q.cu = a.cu_seqlens_q;
+  q.ctx = a.context_lens;
+  q.err = a.err;
+  q.pairs = reinterpret_cast<int4*>(ws + pl.off_pairs);
+  q.units = reinterpret_cast<int4*>(ws + pl.off_units);
+  q.splits = reinterpret_cast<int4*>(ws + pl.off_splits);
+  q.hdr = reinterpret_cast<int32_t*>(ws + pl.off_hdr);
+  q.num_tokens = a.num_tokens;
+  q.B = a.batch;
+  q.TQ = TQ;
+  q.Hkv = d.num_kv_heads;
+  q.n_sm = pl.n_sm;
+  q.max_seqlen_q = a.max_seqlen_q;
+  q.cap_ctx = static_cast<int32_t>(std::min<int64_t>(a.max_context_len, int64_t(a.max_pages) << p.log2P));
+  q.pair_cap = pl.pair_cap;
+  q.slot_cap = pl.slot_cap;
+  q.split_cap = pl.split_cap;
+  prefill_plan_kernel<<<1, kPlanThreads, 0, s>>>(q);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  p.units = q.units;
+  p.n_units = q.hdr;
+  p.lse_part = reinterpret_cast<float*>(ws + pl.off_lse);
+  p.o_part = reinterpret_cast<float*>(ws + pl.off_o);
+  prefill_tc_kernel<<<static_cast<unsigned>(pl.unit_cap) * d.num_kv_heads, kThreads, kSmemBytes, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  if (pl.split_cap > 0) {
+    MergeParams m;
+    m.cu = a.cu_seqlens_q;
+    m.splits = q.splits;
+    m.hdr = q.hdr;
+    m.o_part = p.o_part;
+    m.lse_part = p.lse_part;
+    m.out = p.out;
+    m.Hq = d.num_q_heads;
+    m.Hkv = d.num_kv_heads;
+    m.G = G;
+    m.TQ = TQ;
+    prefill_merge_kernel<<<dim3(pl.split_cap * kMergeRowBlocks, d.num_kv_heads), kMergeThreads, 0, s>>>(m);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace pa

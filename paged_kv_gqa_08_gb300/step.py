@@ -13,8 +13,8 @@ from typing import Optional
 
 import torch
 
-from . import (pa_decode, pa_decode_workspace_size, pa_kv_write, pa_prefill_varlen, pa_qk_norm_rope_kv_write,
-               pa_slot_mapping)
+from . import (pa_decode, pa_decode_workspace_size, pa_kv_write, pa_prefill_varlen, pa_prefill_workspace_size,
+               pa_qk_norm_rope_kv_write, pa_slot_mapping)
 
 
 @dataclasses.dataclass
@@ -23,7 +23,7 @@ class StepBuffers:
     slots: torch.Tensor                # int64 [N]
     out: torch.Tensor                  # [N, Hq, hd]
     q_out: Optional[torch.Tensor]      # [N, Hq, hd] normed + rotated q (when norm weights are used)
-    workspace: Optional[torch.Tensor]  # decode split-KV workspace (bytes)
+    workspace: Optional[torch.Tensor]  # decode split-KV / planned-prefill workspace (bytes)
     max_ctas: int = 0
 
 
@@ -32,7 +32,11 @@ def torch_dtype(desc) -> torch.dtype:
 
 
 def alloc_step_buffers(desc, kind: str, num_tokens: int, batch: int, max_context_len: int, device,
-                       norm: bool = False, max_ctas: int = 0) -> StepBuffers:
+                       norm: bool = False, max_ctas: int = 0, max_seqlen_q: Optional[int] = None,
+                       plan_prefill: bool = True) -> StepBuffers:
+    """Buffers of one step.  A prefill step gets the planned-launch workspace
+    unless ``plan_prefill`` is False (or the shape is never planned); it is
+    sized for chunks up to ``max_seqlen_q`` tokens (default: ``num_tokens``)."""
     dt = torch_dtype(desc)
     n = max(num_tokens, 1)
     positions = torch.empty(n, dtype=torch.int32, device=device)
@@ -45,6 +49,10 @@ def alloc_step_buffers(desc, kind: str, num_tokens: int, batch: int, max_context
         if nbytes == 0:
             raise RuntimeError("pa_decode_workspace_size returned 0 (unsupported shape or no device)")
         ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    elif plan_prefill and num_tokens > 0:
+        nbytes = pa_prefill_workspace_size(desc, batch, max_seqlen_q or num_tokens, num_tokens, max_context_len)
+        if nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
     return StepBuffers(positions, slots, out, q_out, ws, max_ctas)
 
 
@@ -86,5 +94,6 @@ def run_step(desc, kind: str, bufs: StepBuffers, q, k, v, cu_seqlens_q, context_
                   max_context_len, scale, bufs.max_ctas, bufs.out, bufs.workspace, None, stream)
     else:
         pa_prefill_varlen(desc, qa, cu_seqlens_q, batch, max_seqlen_q, n, k_cache, v_cache, block_tables,
-                          max_pages_per_seq, context_lens, max_context_len, scale, bufs.out, stream)
+                          max_pages_per_seq, context_lens, max_context_len, scale, bufs.out, bufs.workspace,
+                          stream=stream)
     return bufs.out

@@ -38,7 +38,8 @@ def as_f64(t: torch.Tensor) -> np.ndarray:
 class GpuRun:
     """All device state of one workload."""
 
-    def __init__(self, wl, device: str = "cuda", max_ctas: int = 0, cache_fill: float = float("nan")):
+    def __init__(self, wl, device: str = "cuda", max_ctas: int = 0, cache_fill: float = float("nan"),
+                 plan_prefill: bool = True):
         self.wl = wl
         self.device = device
         self.t = synth.to_torch(wl, device)
@@ -54,7 +55,8 @@ class GpuRun:
                    self.k_cache, self.v_cache)
         self.bufs = alloc_step_buffers(self.desc, wl.kind, wl.num_new_tokens, wl.batch,
                                        max(wl.max_context_len, 1), device, norm=wl.q_norm_w is not None,
-                                       max_ctas=max_ctas)
+                                       max_ctas=max_ctas, max_seqlen_q=max(wl.max_new_len, 1),
+                                       plan_prefill=plan_prefill)
 
     def step(self) -> torch.Tensor:
         wl, t = self.wl, self.t

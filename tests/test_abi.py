@@ -129,15 +129,27 @@ def test_prefill_argument_validation(lib):
 
     def call(batch=2, maxq=64, n=100, q=FAKE, cu=FAKE, maxp=8, max_ctx=128):
         return lib.pa_prefill_varlen(ctypes.byref(d), q, cu, batch, maxq, n, FAKE, FAKE, FAKE, maxp, FAKE, max_ctx,
-                                     0.1, FAKE, None)
+                                     0.1, FAKE, None, 0, None)
 
     assert call(n=0) == pa.PA_OK
     assert call(batch=0, n=5) == pa.PA_ERR_SHAPE
     assert call(cu=None) == pa.PA_ERR_NULL
     assert call(maxq=200) == pa.PA_ERR_SHAPE      # longer than max_context_len
     assert call(max_ctx=200) == pa.PA_ERR_SHAPE   # beyond max_pages * page_size
+    assert lib.pa_prefill_varlen(ctypes.byref(d), FAKE, FAKE, 2, 64, 100, FAKE, FAKE, FAKE, 8, FAKE, 128, 0.1,
+                                 FAKE, FAKE + 16, 1 << 20, None) == pa.PA_ERR_ALIGN   # workspace wants 256 bytes
     assert lib.pa_prefill_varlen(ctypes.byref(d), FAKE, FAKE, 2, 64, 100, FAKE, FAKE, FAKE, 8, FAKE, 128, -0.1,
-                                 FAKE, None) == pa.PA_ERR_SHAPE       # the scale must be positive
+                                 FAKE, None, 0, None) == pa.PA_ERR_SHAPE       # the scale must be positive
+
+
+def test_prefill_workspace_size_is_zero_when_unused(lib):
+    # fp32 and head_dim 64 run on the CUDA-core kernel, which takes no workspace
+    assert lib.pa_prefill_workspace_size(ctypes.byref(_desc(dtype=pa.PA_F32)), 2, 64, 100, 128) == 0
+    assert lib.pa_prefill_workspace_size(ctypes.byref(_desc(head_dim=64)), 2, 64, 100, 128) == 0
+    # invalid bounds
+    assert lib.pa_prefill_workspace_size(ctypes.byref(_desc()), 0, 64, 100, 128) == 0
+    assert lib.pa_prefill_workspace_size(ctypes.byref(_desc()), 2, 200, 100, 128) == 0
+    assert lib.pa_prefill_workspace_size(None, 2, 64, 100, 128) == 0
 
 
 def test_slot_mapping_and_validate_argument_validation(lib):

@@ -95,3 +95,65 @@ def test_mixed_decode_rows_and_prefill_chunks_in_one_launch():
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
     _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+
+
+def _plan_header(run):
+    """{CTAs per kv-head, split pairs, part size, q-tile pairs} of the last planned call."""
+    return run.bufs.workspace[:16].view(torch.int32).tolist()
+
+
+def test_planned_and_unplanned_launches_agree_on_the_mixed_chunk_batch():
+    wl = synth.make_workload("qwen3_0p6b_chunked_prefill")
+    ref = oracle.reference_step(wl)
+    pa_read_device_errors(reset=True)
+    plain = GpuRun(wl, plan_prefill=False)
+    assert plain.bufs.workspace is None
+    out_plain = plain.step().clone()
+    planned = GpuRun(wl)
+    out_planned = planned.step()
+    torch.cuda.synchronize()
+    units, splits, tau, pairs = _plan_header(planned)
+    assert pairs == 14 and splits > 0 and units > pairs and tau >= 2
+    _check(out_plain[: wl.num_new_tokens], ref["o"], wl.dtype)
+    _check(out_planned[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
+
+
+LONG = [
+    # Hq, Hkv, P, chunks, prefixes: few q-tile pairs over long prefixes, so the
+    # planner cuts each pair's keys into many parts
+    (16, 8, 16, [200], [20000]),
+    (32, 4, 32, [1, 90, 1], [9000, 15000, 31]),    # G = 8; single-row tiles
+    (8, 8, 16, [130, 1], [12000, 6000]),           # G = 1
+]
+
+
+@pytest.mark.parametrize("case", LONG, ids=[f"hq{c[0]}-hkv{c[1]}-chunks{len(c[3])}" for c in LONG])
+def test_split_key_ranges_match_oracle(case):
+    Hq, Hkv, P, chunks, prefixes = case
+    spec = dict(kind="prefill", dtype="bf16", B=len(chunks), Hq=Hq, Hkv=Hkv, hd=128, P=P, chunks=chunks,
+                prefixes=prefixes, norm=True, seed=sum(prefixes) % 1000 + 3)
+    wl = synth.make_workload(spec)
+    pa_read_device_errors(reset=True)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    units, splits, tau, pairs = _plan_header(run)
+    assert splits > 0 and units > pairs
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
+
+
+def test_planned_prefill_with_empty_requests_and_tiny_workload():
+    spec = dict(kind="prefill", dtype="bf16", B=5, Hq=16, Hkv=8, hd=128, P=16, chunks=[0, 3, 0, 1, 0],
+                prefixes=[10, 5000, 0, 1, 7], norm=True, seed=5)
+    wl = synth.make_workload(spec)
+    pa_read_device_errors(reset=True)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    assert _plan_header(run)[3] == 2          # only the two non-empty requests have pairs
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
