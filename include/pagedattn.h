@@ -48,7 +48,8 @@ typedef enum pa_status {
   PA_ERR_UNSUPPORTED = 5, /* well-formed but outside the supported set */
   PA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required */
   PA_ERR_CUDA = 7,        /* a CUDA call or launch failed (pa_last_cuda_error) */
-  PA_ERR_VALIDATION = 8   /* reserved for callers of pa_validate_metadata */
+  PA_ERR_VALIDATION = 8,  /* reserved for callers of pa_validate_metadata */
+  PA_ERR_CAPACITY = 9     /* block manager: not enough free blocks (or host memory) */
 } pa_status;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
@@ -337,6 +338,78 @@ PA_API int32_t pa_last_cuda_error(void);
 
 /* Static description of a status code. */
 PA_API const char* pa_status_string(pa_status status);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager (nano-vLLM learning note: Block, BlockManager,
+ * compute_hash, can_allocate, allocate, deallocate, can_append, may_append and
+ * hash_blocks listings).  Decides which physical page (block) holds each
+ * token of each sequence and shares full pages between sequences whose
+ * prompts start with the same tokens (prefix caching): every full block that
+ * has been computed is registered under a hash of its tokens chained with the
+ * previous block's hash, and a new sequence reuses its leading registered
+ * blocks (never its last block) whose stored tokens match.  Free blocks are a
+ * FIFO: allocation takes the oldest, a released block goes to the back and
+ * keeps its hash until it is handed out again.  Host memory only: the outputs
+ * (block tables, context lengths, slots) are host arrays the caller uploads.
+ * A manager is not thread-safe.  Sequences are named by caller-chosen int64
+ * ids.  The hash is a chained SplitMix64 mix of the 32-bit token ids (the
+ * pages use xxHash64); hits are confirmed by comparing tokens.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager of num_blocks blocks of block_size tokens, all free.  *out is set
+ * to NULL on error.  PA_ERR_CAPACITY if host memory runs out. */
+PA_API pa_status pa_bm_create(int64_t num_blocks, int32_t block_size, pa_block_manager** out);
+PA_API void pa_bm_destroy(pa_block_manager* m);
+
+/* How many leading blocks of a prompt of num_tokens token ids (host) would be
+ * reused from the cache, or -1 in *num_cached_blocks when the free blocks do
+ * not cover the rest.  Changes nothing. */
+PA_API pa_status pa_bm_can_allocate(pa_block_manager* m, const int32_t* token_ids, int64_t num_tokens,
+                                    int64_t* num_cached_blocks);
+
+/* Register sequence seq_id with its prompt and give it ceil(num_tokens /
+ * block_size) blocks, the leading cached ones shared.  *num_cached_tokens
+ * (optional) = tokens whose K/V are already in the shared blocks (a multiple
+ * of block_size): the caller computes and writes only the rest.
+ * PA_ERR_CAPACITY (nothing changed) when the free blocks do not suffice;
+ * PA_ERR_SHAPE when seq_id is already registered. */
+PA_API pa_status pa_bm_allocate(pa_block_manager* m, int64_t seq_id, const int32_t* token_ids, int64_t num_tokens,
+                                int64_t* num_cached_tokens);
+
+/* Append one token (decode); a sequence whose length becomes 1 mod
+ * block_size gets a fresh block.  PA_ERR_CAPACITY (nothing changed) when that
+ * block is not available. */
+PA_API pa_status pa_bm_append_token(pa_block_manager* m, int64_t seq_id, int32_t token_id);
+
+/* Declare the first num_computed_tokens tokens of seq_id computed (their K/V
+ * written): its full blocks among them are registered for prefix reuse. */
+PA_API pa_status pa_bm_hash_blocks(pa_block_manager* m, int64_t seq_id, int64_t num_computed_tokens);
+
+/* Release seq_id: one reference less on each of its blocks, last block first;
+ * blocks nobody holds go to the back of the free list. */
+PA_API pa_status pa_bm_free(pa_block_manager* m, int64_t seq_id);
+
+/* Host int32 block_tables [num_seqs, max_pages_per_seq] for these sequences
+ * (unused entries = pad_page, e.g. a reserved page), and optionally their
+ * lengths in context_lens [num_seqs].  PA_ERR_SHAPE (nothing written) for an
+ * unknown id or a table longer than max_pages_per_seq. */
+PA_API pa_status pa_bm_block_tables(pa_block_manager* m, const int64_t* seq_ids, int32_t num_seqs,
+                                    int32_t max_pages_per_seq, int32_t pad_page, int32_t* block_tables,
+                                    int32_t* context_lens);
+
+/* Host int64 slots of the last num_new_tokens[i] tokens of each sequence, in
+ * order (sum(num_new_tokens) entries): block * block_size + offset, the
+ * values pa_slot_mapping computes on the device. */
+PA_API pa_status pa_bm_slot_mapping(pa_block_manager* m, const int64_t* seq_ids, int32_t num_seqs,
+                                    const int32_t* num_new_tokens, int64_t* slot_mapping);
+
+/* Counters (each output optional). */
+PA_API pa_status pa_bm_query(pa_block_manager* m, int64_t* num_free_blocks, int64_t* num_seqs,
+                             int64_t* num_hashed_blocks);
+PA_API pa_status pa_bm_block_ref_count(pa_block_manager* m, int32_t block_id, int32_t* ref_count);
+PA_API pa_status pa_bm_seq_info(pa_block_manager* m, int64_t seq_id, int64_t* num_tokens,
+                                int64_t* num_cached_tokens, int32_t* num_blocks);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 PA_API int32_t pa_version(void);

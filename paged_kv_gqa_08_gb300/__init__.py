@@ -27,6 +27,7 @@ PA_ERR_UNSUPPORTED = 5
 PA_ERR_WORKSPACE = 6
 PA_ERR_CUDA = 7
 PA_ERR_VALIDATION = 8
+PA_ERR_CAPACITY = 9
 
 PA_F32 = 0
 PA_BF16 = 1
@@ -92,6 +93,18 @@ _SIGS = {
     "pa_last_cuda_error": (_I32, []),
     "pa_status_string": (ctypes.c_char_p, [_I32]),
     "pa_version": (_I32, []),
+    "pa_bm_create": (_I32, [_I64, _I32, ctypes.POINTER(_VP)]),
+    "pa_bm_destroy": (None, [_VP]),
+    "pa_bm_can_allocate": (_I32, [_VP, _VP, _I64, ctypes.POINTER(_I64)]),
+    "pa_bm_allocate": (_I32, [_VP, _I64, _VP, _I64, ctypes.POINTER(_I64)]),
+    "pa_bm_append_token": (_I32, [_VP, _I64, _I32]),
+    "pa_bm_hash_blocks": (_I32, [_VP, _I64, _I64]),
+    "pa_bm_free": (_I32, [_VP, _I64]),
+    "pa_bm_block_tables": (_I32, [_VP, _VP, _I32, _I32, _I32, _VP, _VP]),
+    "pa_bm_slot_mapping": (_I32, [_VP, _VP, _I32, _VP, _VP]),
+    "pa_bm_query": (_I32, [_VP, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "pa_bm_block_ref_count": (_I32, [_VP, _I32, ctypes.POINTER(_I32)]),
+    "pa_bm_seq_info": (_I32, [_VP, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I32)]),
 }
 
 

@@ -1,6 +1,6 @@
 """Build libpagedattn.so in-tree with nvcc (sm_103a only).
 
-Each ``csrc/*.cu`` file is compiled to an object in ``_build/`` in parallel,
+Each ``csrc/*.cu`` (and host-only ``*.cpp``) file is compiled to an object in ``_build/`` in parallel,
 then linked into ``lib/libpagedattn.so`` with the CUDA runtime linked
 statically and only the ``pa_*`` entry points exported.  Rebuilds only what
 is out of date.  ``python -m paged_kv_gqa_08_gb300.build`` runs it.
@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _headers():
@@ -65,7 +65,7 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
     work = []
     objs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         if force or _mtime(obj) < max(_mtime(src), newest_header):
             work.append((src, obj))

@@ -452,10 +452,11 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_WORKSPACE: return "workspace missing or too small";
     case PA_ERR_CUDA: return "CUDA error";
     case PA_ERR_VALIDATION: return "metadata validation failed";
+    case PA_ERR_CAPACITY: return "not enough free blocks";
   }
   return "unknown status";
 }
 
-int32_t pa_version(void) { return 100; }
+int32_t pa_version(void) { return 200; }
 
 }  // extern "C"

@@ -43,7 +43,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_version_and_status_strings(lib):
     assert pa.pa_version() >= 100
-    for s in range(0, 9):
+    for s in range(0, 10):
         assert pa.pa_status_string(s)
     assert pa.pa_status_string(12345) == "unknown status"
 
