@@ -87,6 +87,7 @@ struct KParams {
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams p) {
   __shared__ int32_t warp_tot[kPlanThreads / 32];
   __shared__ int32_t carry;
+  pdl_trigger();  // the decode kernel may start launching; it waits for this plan
   const int tid = threadIdx.x;
   const int T = 1 << p.log2T;
   const int cap = min(p.max_ctx, p.maxp << p.log2P);
@@ -226,6 +227,8 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
   const int NW = p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  pdl_wait();     // the plan kernel's chunk sums and CTA starts are complete
+  pdl_trigger();  // the merge kernel may start launching; it waits for this grid
   const int NC = p.cs[p.B];
   const int x0 = static_cast<int>((static_cast<int64_t>(c) * NC) / p.n_ctas);
   const int x1 = static_cast<int>((static_cast<int64_t>(c + 1) * NC) / p.n_ctas);
@@ -515,6 +518,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
 template <typename T, int HD>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const KParams p) {
   constexpr int EL = HD / 32;  // elements per lane
+  pdl_wait();                  // every partial of the decode grid is written
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + warp;
   if (u >= static_cast<int64_t>(p.B) * p.Hq) return;
@@ -757,14 +761,18 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   p.v_new_stride = a.v_new_stride_bytes;
   p.slot_out = a.slot_out;
 
+  // plan -> decode -> merge, the last two launched to overlap their launch with
+  // the kernel before them (each waits for it before reading its output)
   decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), args, pl.smem_bytes, s);
+  e = launch_after_previous(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), pl.smem_bytes, s, args);
   if (e != cudaSuccess) return e;
   if (pl.n_ctas > 1) {
     const int64_t pairs = static_cast<int64_t>(a.batch) * d.num_q_heads;
     const unsigned blocks = static_cast<unsigned>((pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
-    e = cudaLaunchKernel(f.merge, dim3(blocks), dim3(kMergeThreads), args, 0, s);
+    e = launch_after_previous(f.merge, dim3(blocks), dim3(kMergeThreads), 0, s, args);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();

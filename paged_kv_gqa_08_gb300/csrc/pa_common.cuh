@@ -125,6 +125,16 @@ PA_DEVINL void bulk_g2s_hint(void* dst_smem, const void* src_gmem, uint32_t byte
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream still runs;
+// pdl_wait() returns once that kernel has completed and its writes are visible
+// (at once when the launch had no such dependency).  pdl_trigger() lets the
+// next kernel of the stream start launching.
+// ----------------------------------------------------------------------------
+PA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+PA_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------
 // named barriers (subset of warps)
 // ----------------------------------------------------------------------------
 PA_DEVINL void named_bar_sync(int id, int nthreads) {

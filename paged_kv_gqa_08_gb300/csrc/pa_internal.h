@@ -117,6 +117,24 @@ struct DecodeArgs {
 cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& plan, const DecodeArgs& a,
                           cudaStream_t s);
 
+// Launch `fn` so that it may start while the stream's previous kernel runs
+// (programmatic stream serialisation); the kernel calls pdl_wait() before it
+// reads anything that kernel writes.
+inline cudaError_t launch_after_previous(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                         void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // ---------------------------------------------------------------------------
 // prefill
 // ---------------------------------------------------------------------------

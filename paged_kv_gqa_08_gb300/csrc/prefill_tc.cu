@@ -232,6 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   int h, b, qp, j_lo = 0, j_hi = 1 << 30, slot = -1;
   if (p.units) {
+    pdl_wait();     // the planner's unit list is complete
+    pdl_trigger();  // the merge kernel may start launching; it waits for this grid
     const int u = static_cast<int>(blockIdx.x) / p.Hkv;
     h = static_cast<int>(blockIdx.x) - u * p.Hkv;
     if (u >= *p.n_units) return;
@@ -683,6 +685,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
   __shared__ float cand_est[kPlanCandidates];
   __shared__ int cand_tau[kPlanCandidates];
   __shared__ int sh_max_nt, sh_tau;
+  pdl_trigger();  // the attention kernel may start launching; it waits for this plan
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) sh_max_nt = 0;
   for (int i = tid; i < kPlanBuckets; i += kPlanThreads) cursor[i] = 0;
@@ -860,6 +863,7 @@ struct MergeParams {
 // The parts' log-sum-exps are loaded one per lane and reduced by shuffles;
 // the O loads of four parts are in flight together.
 __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const MergeParams m) {
+  pdl_wait();  // every part of the attention grid is written
   const int si = blockIdx.x / kMergeRowBlocks, h = blockIdx.y;
   if (si >= m.hdr[1]) return;
   const int4 sp = m.splits[si];
@@ -1073,8 +1077,13 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   p.n_units = q.hdr;
   p.lse_part = reinterpret_cast<float*>(ws + pl.off_lse);
   p.o_part = reinterpret_cast<float*>(ws + pl.off_o);
-  prefill_tc_kernel<<<static_cast<unsigned>(pl.unit_cap) * d.num_kv_heads, kThreads, kSmemBytes, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    void* args[] = {&p};
+    e = launch_after_previous(reinterpret_cast<const void*>(prefill_tc_kernel),
+                              dim3(static_cast<unsigned>(pl.unit_cap) * d.num_kv_heads), dim3(kThreads), kSmemBytes, s,
+                              args);
+    if (e != cudaSuccess) return e;
+  }
 
   if (pl.split_cap > 0) {
     MergeParams m;
@@ -1088,8 +1097,10 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
     m.Hkv = d.num_kv_heads;
     m.G = G;
     m.TQ = TQ;
-    prefill_merge_kernel<<<dim3(pl.split_cap * kMergeRowBlocks, d.num_kv_heads), kMergeThreads, 0, s>>>(m);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    void* args[] = {&m};
+    e = launch_after_previous(reinterpret_cast<const void*>(prefill_merge_kernel),
+                              dim3(pl.split_cap * kMergeRowBlocks, d.num_kv_heads), dim3(kMergeThreads), 0, s, args);
+    if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
