@@ -72,6 +72,7 @@ struct KParams {
   uint32_t off_bar, off_meta, off_p, off_alpha, off_ml, off_abort;
   int32_t p_row;        // floats per token row of the probability tile
   float scale_log2;     // softmax scale * log2(e)
+  int32_t merge_w;      // warps per (request, q-head) in the merge kernel: 1, 2 or 4
   // Fused KV write (k_new != nullptr): the new token of request b is row b of
   // k_new / v_new; it is attended from there and stored into its cache slot
   // (position context_lens[b] - 1) by the CTA that owns the request's last chunk.
@@ -511,61 +512,99 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
 }
 
 // ---------------------------------------------------------------------------
-// log-sum-exp merge of the partials of requests cut across CTAs.  One warp per
-// (request, q-head); a lane owns HD/32 elements of the head; the loop over the
-// partials keeps several independent loads in flight.
+// log-sum-exp merge of the partials of requests cut across CTAs.  merge_w
+// warps per (request, q-head): each takes a contiguous range of the partials,
+// a lane owns HD/32 elements of the head, the partials' weights are computed
+// one per lane and eight partials' loads are in flight together; the warps'
+// sums meet in shared memory and are added in a fixed order.
 // ---------------------------------------------------------------------------
 template <typename T, int HD>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const KParams p) {
   constexpr int EL = HD / 32;  // elements per lane
+  constexpr int NWARP = kMergeThreads / 32;
+  __shared__ float red[NWARP][32][EL + 1];
   pdl_wait();                  // every partial of the decode grid is written
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t u = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + warp;
-  if (u >= static_cast<int64_t>(p.B) * p.Hq) return;
-  const int b = static_cast<int>(u / p.Hq), hq = static_cast<int>(u - static_cast<int64_t>(b) * p.Hq);
-  const int NC = p.cs[p.B];
-  const int cb0 = p.cs[b], cb1 = p.cs[b + 1];
-  if (cb1 <= cb0) return;
-  auto start = [&](int c) { return (static_cast<int64_t>(c) * NC) / p.n_ctas; };
-  const int c0 = static_cast<int>(((static_cast<int64_t>(cb0) + 1) * p.n_ctas + NC - 1) / NC) - 1;
-  const int c1 = static_cast<int>(((static_cast<int64_t>(cb1)) * p.n_ctas + NC - 1) / NC) - 1;
-  if (c0 == c1) return;  // written whole by its CTA
+  const int W = p.merge_w, item = warp / W, sub = warp - item * W;
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * (NWARP / W) + item;
+  // The W warps of an item decide together; no warp leaves before the CTA
+  // barrier below (merge_w, and so the barrier, is the same for every CTA).
+  int b = 0, hq = 0, c0 = 0, parts = 0, NC = 0;
+  bool active = u < static_cast<int64_t>(p.B) * p.Hq;
+  if (active) {
+    b = static_cast<int>(u / p.Hq);
+    hq = static_cast<int>(u - static_cast<int64_t>(b) * p.Hq);
+    NC = p.cs[p.B];
+    const int cb0 = p.cs[b], cb1 = p.cs[b + 1];
+    if (cb1 <= cb0) {
+      active = false;
+    } else {
+      c0 = static_cast<int>(((static_cast<int64_t>(cb0) + 1) * p.n_ctas + NC - 1) / NC) - 1;
+      const int c1 = static_cast<int>(((static_cast<int64_t>(cb1)) * p.n_ctas + NC - 1) / NC) - 1;
+      parts = c1 - c0 + 1;
+      active = c0 != c1;  // one CTA wrote the request whole
+    }
+  }
   // With more CTAs than chunks some CTAs between c0 and c1 own no chunk and
-  // wrote no partial: only CTAs with a non-empty range take part.
-  float M = -INFINITY;
-  for (int cc = c0 + lane; cc <= c1; cc += 32)
-    if (start(cc) < start(cc + 1)) M = fmaxf(M, p.lse_part[(static_cast<int64_t>(cc) + b) * p.Hq + hq]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // wrote no partial: only CTAs with a non-empty range take part.  With at
+  // least as many chunks as CTAs every CTA has a range.
+  const bool all_busy = NC >= p.n_ctas;
+  auto start = [&](int c) { return (static_cast<int64_t>(c) * NC) / p.n_ctas; };
+  auto busy = [&](int cc) { return all_busy || start(cc) < start(cc + 1); };
+  auto lse_of = [&](int k) { return p.lse_part[(static_cast<int64_t>(c0 + k) + b) * p.Hq + hq]; };
   float acc[EL];
 #pragma unroll
   for (int e = 0; e < EL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  if (M != -INFINITY) {
-    int64_t s_lo = start(c0);
-#pragma unroll 4
-    for (int cc = c0; cc <= c1; ++cc) {
-      const int64_t s_hi = start(cc + 1);
-      const bool busy = s_lo < s_hi;
-      s_lo = s_hi;
-      if (!busy) continue;
-      const int64_t slot = static_cast<int64_t>(cc) + b;
-      const float w = exp2f(p.lse_part[slot * p.Hq + hq] - M);
-      const float* src = p.o_part + (slot * p.Hq + hq) * HD + lane * EL;
-      if constexpr (EL == 4) {
-        const float4 ov = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * ov.x;
-        acc[1] += w * ov.y;
-        acc[2] += w * ov.z;
-        acc[3] += w * ov.w;
-      } else {
-        const float2 ov = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * ov.x;
-        acc[1] += w * ov.y;
+  if (active) {
+    float M = -INFINITY;
+    for (int k = lane; k < parts; k += 32)
+      if (busy(c0 + k)) M = fmaxf(M, lse_of(k));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const int per = (parts + W - 1) / W;
+    const int k_begin = sub * per, k_end = min(parts, k_begin + per);
+    if (M != -INFINITY) {
+      for (int k0 = k_begin; k0 < k_end; k0 += 32) {
+        const int k = k0 + lane;
+        const float w_mine = k < k_end && busy(c0 + k) ? exp2f(lse_of(k) - M) : 0.f;
+        const int kn = min(32, k_end - k0);
+#pragma unroll 8
+        for (int i = 0; i < kn; ++i) {
+          const float w = __shfl_sync(0xffffffffu, w_mine, i);
+          const int64_t slot = static_cast<int64_t>(c0 + k0 + i) + b;
+          const float* src = p.o_part + (slot * p.Hq + hq) * HD + lane * EL;
+          if (w != 0.f) {
+            if constexpr (EL == 4) {
+              const float4 ov = *reinterpret_cast<const float4*>(src);
+              acc[0] += w * ov.x;
+              acc[1] += w * ov.y;
+              acc[2] += w * ov.z;
+              acc[3] += w * ov.w;
+            } else {
+              const float2 ov = *reinterpret_cast<const float2*>(src);
+              acc[0] += w * ov.x;
+              acc[1] += w * ov.y;
+            }
+            wsum += w;
+          }
+        }
       }
-      wsum += w;
     }
   }
+  if (W > 1) {
+#pragma unroll
+    for (int e = 0; e < EL; ++e) red[warp][lane][e] = acc[e];
+    red[warp][lane][EL] = wsum;
+    __syncthreads();
+    if (sub != 0) return;
+    for (int w2 = 1; w2 < W; ++w2) {
+#pragma unroll
+      for (int e = 0; e < EL; ++e) acc[e] += red[warp + w2][lane][e];
+      wsum += red[warp + w2][lane][EL];
+    }
+  }
+  if (!active) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const int64_t e0 = (static_cast<int64_t>(b) * p.Hq + hq) * HD + lane * EL;
   if constexpr (sizeof(T) == 2) {
@@ -770,8 +809,13 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   e = launch_after_previous(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), pl.smem_bytes, s, args);
   if (e != cudaSuccess) return e;
   if (pl.n_ctas > 1) {
+    // warps per (request, q-head): about one per 8 partials of a request when
+    // the requests are equally long (CTAs per request / 8), at most 4
+    const int per_req = pl.n_ctas / std::max(1, a.batch);
+    p.merge_w = per_req >= 32 ? 4 : per_req >= 16 ? 2 : 1;
     const int64_t pairs = static_cast<int64_t>(a.batch) * d.num_q_heads;
-    const unsigned blocks = static_cast<unsigned>((pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
+    const int items = kMergeThreads / 32 / p.merge_w;
+    const unsigned blocks = static_cast<unsigned>((pairs + items - 1) / items);
     e = launch_after_previous(f.merge, dim3(blocks), dim3(kMergeThreads), 0, s, args);
     if (e != cudaSuccess) return e;
   }
