@@ -533,8 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(x[64 * hh + 2 * e]), p.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(x[64 * hh + 2 * e + 1]), p.scale_log2, neg_m));
+          const float2 t = ffma2(make_float2(__uint_as_float(x[64 * hh + 2 * e]), __uint_as_float(x[64 * hh + 2 * e + 1])),
+                                 make_float2(p.scale_log2, p.scale_log2), make_float2(neg_m, neg_m));
+          const float p0 = ex2(t.x);
+          const float p1 = ex2(t.y);
           rs4[e & 3] = fadd2(rs4[e & 3], make_float2(p0, p1));
           w[e] = pack_bf16x2(p0, p1);
         }
