@@ -37,6 +37,7 @@
 // parts of each split pair (flash-decoding's split-KV rule, applied to
 // prefill rows).
 #include <cuda.h>
+#include <limits.h>
 #include <math.h>
 #include <string.h>
 
@@ -340,23 +341,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int64_t bt_row = static_cast<int64_t>(b) * p.maxp;
     const int box = lane >> 2, half = (lane >> 1) & 1, isv = lane & 1;
     const int x = h * 128 + half * 64;
+    // Block-table entries are read one tile ahead: the loads for tile j + 1
+    // are issued before tile j's stage waits, so their latency is hidden
+    // behind them.  kNoPage marks an entry the lane does not need.
+    constexpr int kNoPage = INT_MIN;
+    auto load_pages = [&](int jj, int& pg_full, int& pg_rem) {
+      const int t0 = (j_lo + jj) * kBN;
+      const int valid = min(kBN, kv_len - t0);
+      const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+      pg_full = box < nfull ? p.bt[bt_row + ((t0 + box * kBoxRows) >> p.log2P)] : kNoPage;
+      pg_rem = rem && lane < 4 ? p.bt[bt_row + ((t0 + nfull * kBoxRows) >> p.log2P)] : kNoPage;
+    };
+    int pf_next = kNoPage, pr_next = kNoPage;
+    if (nt > 0) load_pages(0, pf_next, pr_next);
     for (int j = 0; j < nt && ok; ++j) {
       const int st = j & 1;
       const uint32_t par = ((j >> 1) & 1) ^ 1;
       const int t0 = (j_lo + j) * kBN;
       const int valid = min(kBN, kv_len - t0);
       const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+      const int pf = pf_next, pr = pr_next;
+      if (j + 1 < nt) load_pages(j + 1, pf_next, pr_next);
       int y_full = -1, y_rem = -1;
-      if (box < nfull) {
+      if (pf != kNoPage) {
         const int key0 = t0 + box * kBoxRows;
-        const int page = p.bt[bt_row + (key0 >> p.log2P)];
-        if (page >= 0 && page < p.num_pages) y_full = (page << p.log2P) + (key0 & (p.P - 1));
+        if (pf >= 0 && pf < p.num_pages) y_full = (pf << p.log2P) + (key0 & (p.P - 1));
         else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
       }
-      if (rem && lane < 4) {
+      if (pr != kNoPage) {
         const int key0 = t0 + nfull * kBoxRows;
-        const int page = p.bt[bt_row + (key0 >> p.log2P)];
-        if (page >= 0 && page < p.num_pages) y_rem = (page << p.log2P) + (key0 & (p.P - 1));
+        if (pr >= 0 && pr < p.num_pages) y_rem = (pr << p.log2P) + (key0 & (p.P - 1));
         else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
       }
       uint32_t mine = (y_full >= 0 ? kBoxRows * 128 : 0) + (y_rem >= 0 ? rem * 128 : 0);
