@@ -11,10 +11,12 @@
 // TQ = 128 / G tokens x the G q-heads that share the kv-head, so each staged
 // K/V tile feeds the whole GQA group, and it feeds both q-tiles of the pair
 // (256 rows per K/V tile).
-//   warp 0     TMA producer: both Q tiles once (3-D map), then per 128-key tile
-//              the K and V rows gathered page by page with 16-row boxes
+//   warp 0     TMA producer of Q and K: both Q tiles once (3-D map), then per
+//              128-key tile the K rows gathered page by page with 16-row boxes
 //              (single-row boxes for a ragged end, so no slot past the context
-//              is read).
+//              is read); block-table entries are read one tile ahead.
+//   warp 10    TMA producer of V, the same way; K and V run ahead of the MMAs
+//              independently, each as far as its own two stages allow.
 //   warp 1     allocates all 512 TMEM columns; lane 0 issues the MMAs:
 //              S_g = Q_g K_j^T and O_g += P_g V_j for the two q-tiles g, in
 //              the order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), so that each
@@ -53,7 +55,8 @@ constexpr int kBM = 128;                    // rows per q-tile
 constexpr int kBN = 128;                    // keys per tile
 constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 bf16 (one swizzle-atom column)
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;  // warp 0 K copies, 1 MMA, 2-9 softmax, 10 V copies
+constexpr int kVWarp = 10;
 constexpr int kBoxRows = 16;
 constexpr uint32_t kTmemCols = 512;
 
@@ -326,11 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
-    // ------------------------------- TMA producer -------------------------------
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------- TMA producers -------------------------------
+    // warp 0 copies Q and the K tiles, warp kVWarp the V tiles; each runs ahead
+    // as far as its own stages allow
+    const bool vrole = warp == kVWarp;
     int issued_k = 0, issued_v = 0;
     bool ok = true;
-    if (lane == 0) {
+    if (lane == 0 && !vrole) {
       mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nq * 2 * p.G * p.TQ * 128));
       for (int g = 0; g < nq; ++g) {
         const int z = s0 + (2 * qp + g) * p.TQ;
@@ -380,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         kb += __shfl_xor_sync(0xffffffffu, kb, o);
         vb += __shfl_xor_sync(0xffffffffu, vb, o);
       }
+      if (!vrole) {
       int okk = 1;
       if (lane == 0) {
         okk = mbar_wait_bounded(&k_empty[st], par, abort_flag, p.err);
@@ -394,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, &p.tm_k1, x, y_rem + r, &k_full[st]);
       }
       ++issued_k;
+      } else {
       int okv = 1;
       if (lane == 0) {
         okv = mbar_wait_bounded(&v_empty[st], par, abort_flag, p.err);
@@ -408,9 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, &p.tm_v1, x, y_rem + r, &v_full[st]);
       }
       ++issued_v;
+      }
     }
     if (!ok && lane == 0) {
-      drain(q_full, 0);
+      if (!vrole) drain(q_full, 0);
       for (int j = max(0, issued_k - 2); j < issued_k; ++j) drain(&k_full[j & 1], (j >> 1) & 1);
       for (int j = max(0, issued_v - 2); j < issued_v; ++j) drain(&v_full[j & 1], (j >> 1) & 1);
     }
