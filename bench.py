@@ -406,15 +406,28 @@ def time_e2e(d: Device, steps: int, warmup: int, world: int):
     host memory to the device, runs, and reads the result back to the host."""
     wl, t = d.wl, d.t
     names = ["q", "k_new", "v_new", "context_lens", "cu_seqlens_q", "block_tables"]
-    host = {k: t[k].cpu().pin_memory() for k in names}
-    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    # The step's inputs live in one device buffer (256-byte aligned views) filled
+    # from one pinned host buffer of the same layout: one host-to-device copy
+    # per step instead of one per input.
+    offs, total = {}, 0
+    for k in names:
+        offs[k] = total
+        total += (t[k].numel() * t[k].element_size() + 255) // 256 * 256
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=t["q"].device)
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for k in names:
+        nb = t[k].numel() * t[k].element_size()
+        view = dev_buf[offs[k]:offs[k] + nb].view(t[k].dtype).view(t[k].shape)
+        view.copy_(t[k])
+        host_buf[offs[k]:offs[k] + nb].copy_(t[k].contiguous().view(-1).view(torch.uint8).cpu())
+        t[k] = view
+    h2d = sum(t[k].numel() * t[k].element_size() for k in names)
     n = wl.num_new_tokens
     out_host = torch.empty((n,) + tuple(d.bufs.out.shape[1:]), dtype=d.bufs.out.dtype).pin_memory()
     d2h = out_host.numel() * out_host.element_size()
 
     def body():
-        for k in names:
-            t[k].copy_(host[k], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         d.write_part()
         d.attn_part()
         out_host.copy_(d.bufs.out[:n], non_blocking=True)
