@@ -157,3 +157,30 @@ def test_planned_prefill_with_empty_requests_and_tiny_workload():
     ref = oracle.reference_step(wl)
     _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
     assert pa_read_device_errors(reset=True) == 0
+
+
+# Random batches through the planned launch: group sizes 1-8, page sizes 16-256,
+# chunk and prefix mixes that make the planner split some pairs (few pairs over
+# long prefixes) and not others; every case against the oracle.
+RANDOM_CASES = 12
+
+
+@pytest.mark.parametrize("seed", range(RANDOM_CASES))
+def test_random_planned_batches_match_oracle(seed):
+    rng = np.random.default_rng(1000 + seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    P = int(rng.choice([16, 32, 64, 256]))
+    B = int(rng.integers(1, 6))
+    chunks = [int(c) for c in rng.choice([1, 3, 17, 64, 100, 250], size=B)]
+    prefixes = [int(x) for x in rng.integers(0, 3000, size=B)]
+    spec = dict(kind="prefill", dtype="bf16", B=B, Hq=Hkv * G, Hkv=Hkv, hd=128, P=P, chunks=chunks,
+                prefixes=prefixes, norm=bool(seed % 2), seed=seed + 50)
+    wl = synth.make_workload(spec)
+    pa_read_device_errors(reset=True)
+    run = GpuRun(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
