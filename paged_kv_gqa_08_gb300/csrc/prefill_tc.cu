@@ -22,11 +22,12 @@
 //              the order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), so that each
 //              softmax group has a PV and a QK of the other group to hide in.
 //   warps 2-9  two softmax groups of 4 warps, one thread per row (= TMEM
-//              lane): pass 1 reads S and takes the row max; O in TMEM is
-//              rescaled only when a row max grows by more than 2^8; pass 2
-//              reads S again, turns it into bf16 probabilities and writes them
-//              back over S's first 64 columns, where the PV MMA reads its A
-//              operand.  Finally O / l goes to global memory.
+//              lane): a tile's 128 scores come into registers in one TMEM
+//              round trip, the row max is taken, O in TMEM is rescaled only
+//              when a row max grows by more than 2^8, and the bf16
+//              probabilities are written back over S's first 64 columns,
+//              where the PV MMA reads its A operand.  Finally O / l goes to
+//              global memory.
 // TMEM: S_0 cols 0-127 (P_0 in 0-63), S_1 128-255 (P_1 in 128-191),
 //       O_0 256-383, O_1 384-511.
 // Every wait is bounded; a timeout raises PA_DEVERR_TIMEOUT and the CTA
