@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
   pdl_trigger();  // the decode kernel may start launching; it waits for this plan
   const int tid = threadIdx.x;
   const int T = 1 << p.log2T;
-  const int cap = min(p.max_ctx, p.maxp << p.log2P);
+  const int cap = static_cast<int>(min(static_cast<int64_t>(p.max_ctx), static_cast<int64_t>(p.maxp) << p.log2P));
   if (tid == 0) carry = 0;
   __syncthreads();
   for (int base = 0; base < p.B; base += kPlanThreads) {

@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int n = s1 - s0;
   if (2 * qp * p.TQ >= n) return;
   const int L = p.ctx[b];
-  const int cap = min(p.max_ctx, p.maxp << p.log2P);
+  const int cap = static_cast<int>(min(static_cast<int64_t>(p.max_ctx), static_cast<int64_t>(p.maxp) << p.log2P));
   if (s0 < 0 || s1 > p.num_tokens || L < n || L > cap) {
     if (threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
     return;
