@@ -115,15 +115,26 @@ __global__ void __launch_bounds__(128) norm_rope_kv_write_kernel(const NormRopeP
   const bool slot_ok = slot >= 0 && slot < p.num_slots;
   if (!slot_ok && slot != -1 && threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_SLOT);
 
-  // cos / sin of this lane's pair indices: the angle pos * theta^(-2i/HD) is
-  // formed and reduced modulo 2*pi in double, then evaluated in float.
+  // cos / sin of the token's HD/2 pair indices, once per token (one thread
+  // per pair; fp64 is slow on this GPU, so it is not repeated per lane): the
+  // angle pos * theta^(-2i/HD) is formed and reduced modulo 2*pi in double,
+  // then evaluated in float.
+  __shared__ float cs_s[HD / 2], sn_s[HD / 2];
+  if (threadIdx.x < HD / 2) {
+    const double ang = static_cast<double>(pos) * p.inv_freq[threadIdx.x];
+    const double k = rint(ang * (1.0 / kTwoPiHi));
+    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
+    float sv, cv;
+    sincosf(static_cast<float>(r), &sv, &cv);
+    cs_s[threadIdx.x] = cv;
+    sn_s[threadIdx.x] = sv;
+  }
+  __syncthreads();
   float cs[PE], sn[PE];
 #pragma unroll
   for (int e = 0; e < PE; ++e) {
-    const double ang = static_cast<double>(pos) * p.inv_freq[l * PE + e];
-    const double k = rint(ang * (1.0 / kTwoPiHi));
-    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
-    sincosf(static_cast<float>(r), &sn[e], &cs[e]);
+    cs[e] = cs_s[l * PE + e];
+    sn[e] = sn_s[l * PE + e];
   }
   float wq_a[PE], wq_b[PE], wk_a[PE], wk_b[PE];
   Vec4<T>::load(static_cast<const T*>(p.wq) + l * PE, wq_a);
