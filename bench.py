@@ -393,6 +393,24 @@ def time_graph_parts(d: Device, steps: int, warmup: int, flush=None):
     return write_ms + attn_ms, write_ms, attn_ms
 
 
+def step_percentiles(d: Device, n: int = 100):
+    """p10 / p50 / p90 of single graph-replayed steps (CUDA events around each
+    replay), taken after the timed region."""
+    g = capture_graph(lambda: (d.write_part(), d.attn_part()))
+    for _ in range(5):
+        g.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    t = np.sort(np.array([a.elapsed_time(b) for a, b in ev]))
+    return {"p10": float(t[int(0.1 * (n - 1))]), "p50": float(t[int(0.5 * (n - 1))]), "p90": float(t[int(0.9 * (n - 1))]),
+            "replays": n}
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -641,6 +659,7 @@ def main():
         "gpu_launches": launches,
         "decode_partitions": n_parts,
         "clocks": clocks.summary(),
+        "step_ms_percentiles": step_percentiles(d),
     }
     del d
     torch.cuda.empty_cache()
