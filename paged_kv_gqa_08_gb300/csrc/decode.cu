@@ -169,6 +169,32 @@ struct Butterfly {
   }
 };
 
+// The halving levels of Butterfly alone (CUR values -> 1 over lane bits M,
+// M/2, ...), for reducing a sub-array whose levels come first.
+template <int CUR, int M>
+struct Halve {
+  template <int N>
+  static PA_DEVINL void run(float (&a)[N], int lane) {
+    if constexpr (CUR >= 2) {
+      static_assert(M >= 1, "one lane bit per halving level");
+      constexpr int H = CUR / 2;
+      const bool upper = (lane & M) != 0;
+#pragma unroll
+      for (int u = 0; u < H; ++u) {
+        const float send = upper ? a[u] : a[u + H];
+        const float keep = upper ? a[u + H] : a[u];
+        a[u] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+      }
+      Halve<H, M / 2>::run(a, lane);
+    }
+  }
+};
+
+// Floats per token row of the probability tile: each probability is stored
+// twice, (p, p), so that the PV products read ready-made fp32 pairs, and the
+// row is padded to whole 16-byte vectors.
+__host__ __device__ constexpr int p_row_floats(int G) { return 2 * (G <= 2 ? 2 : G <= 4 ? 4 : 8); }
+
 template <typename T, int NPR>
 PA_DEVINL void unpack16(const uint4 w, float2 (&f)[NPR]) {
   if constexpr (sizeof(T) == 2) {
@@ -221,7 +247,10 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
   constexpr int VF = VP >= LPR ? VP / LPR : 1;          // values a lane keeps
   constexpr int DUP = VP >= LPR ? 0 : ilog2c(LPR / VP);  // low lane bits holding copies
   constexpr int IBITS = ilog2c(kTPL / VF);               // lane bits carrying the token index
+  constexpr int GP = VP / kTPL;                          // heads padded to a power of two
+  constexpr int PR = p_row_floats(G);
   static_assert(VF <= kTPL, "a lane's values must share one head");
+  static_assert(GP <= LPR, "the head levels of the reduction fit in a row's lanes");
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int c = blockIdx.x;
@@ -340,7 +369,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
   const int i_l0 = vbase % kTPL;         // token index of its first kept value
   const bool writer = (j & ((1 << DUP) - 1)) == 0;
   const bool head_leader = writer && rs == 0 && (((j >> DUP) & ((1 << IBITS) - 1)) == 0) && g_l < G;
-  float* p_tile = reinterpret_cast<float*>(smem + p.off_p) + warp * Gm::TOK * p.p_row;
+  float* p_tile = reinterpret_cast<float*>(smem + p.off_p) + warp * Gm::TOK * PR;
   float* alpha_s = reinterpret_cast<float*>(smem + p.off_alpha) + warp * 8;
   float* ml_s = reinterpret_cast<float*>(smem + p.off_ml) + warp * 16;
 
@@ -384,24 +413,33 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
       }
     }
 
-    // scores: partial dot products over this lane's 16 bytes of each row
-    float a[VP];
+    // scores: partial dot products over this lane's 16 bytes of each row,
+    // reduced over the row's lanes by a halving butterfly.  The score of
+    // (head g, token i) is value g * kTPL + i, and the butterfly halves the
+    // highest value bit first, so its first log2(GP) levels pair heads of one
+    // token: they run per token, right after that token's products.
+    float a[kTPL];
 #pragma unroll
     for (int i = 0; i < kTPL; ++i) {
       const int t = i * RPI + rs;
       float2 kf[NPR];
       unpack16<T, NPR>(*reinterpret_cast<const uint4*>(kbuf + t * p.row_bytes), kf);
+      float b[GP];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float2 acc = make_float2(0.f, 0.f);
+      for (int g = 0; g < GP; ++g) {
+        if (g < G) {
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int r = 0; r < NPR; ++r) acc = ffma2(qf[g][r], kf[r], acc);
-        a[g * kTPL + i] = acc.x + acc.y;
+          for (int r = 0; r < NPR; ++r) acc = ffma2(qf[g][r], kf[r], acc);
+          b[g] = acc.x + acc.y;
+        } else {
+          b[g] = 0.f;
+        }
       }
+      Halve<GP, LPR / 2>::run(b, lane);
+      a[i] = b[0];
     }
-#pragma unroll
-    for (int v = V; v < VP; ++v) a[v] = 0.f;
-    Butterfly<VP, LPR / 2>::run(a, lane);
+    if constexpr (LPR / (2 * GP) >= 1) Butterfly<kTPL, LPR / (2 * GP)>::run(a, lane);
 
     // online softmax (base 2) for the lane's head
     float sc[VF];
@@ -424,7 +462,8 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
     for (int u = 0; u < VF; ++u) {
       const float pv = exp2f(sc[u] - m_use);
       psum += pv;
-      if (writer && g_l < G) p_tile[((i_l0 + u) * RPI + rs) * p.p_row + g_l] = pv;
+      if (writer && g_l < G)
+        *reinterpret_cast<float2*>(p_tile + ((i_l0 + u) * RPI + rs) * PR + 2 * g_l) = make_float2(pv, pv);
     }
     l_run = l_run * alpha + psum;
     m_run = m_new;
@@ -434,9 +473,14 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
     bool rescale = false;
     float al[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      al[g] = alpha_s[g];
-      rescale |= al[g] != 1.f;
+    for (int g4 = 0; g4 < G; g4 += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + g4);
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int g = g4; g < G && g < g4 + 4; ++g) {
+        al[g] = av[g - g4];
+        rescale |= al[g] != 1.f;
+      }
     }
     if (rescale) {
 #pragma unroll
@@ -452,13 +496,18 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
       if (t < n) {
         float2 vf[NPR];
         unpack16<T, NPR>(*reinterpret_cast<const uint4*>(vbuf + t * p.row_bytes), vf);
-        const float* prow = p_tile + t * p.p_row;
+        const float4* prow = reinterpret_cast<const float4*>(p_tile + t * PR);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pg = prow[g];
-          const float2 pp = make_float2(pg, pg);
+        for (int g2 = 0; g2 < G; g2 += 2) {
+          const float4 pv2 = prow[g2 / 2];  // (p_g, p_g, p_g+1, p_g+1)
+          const float2 pp0 = make_float2(pv2.x, pv2.y);
 #pragma unroll
-          for (int r = 0; r < NPR; ++r) o[g][r] = ffma2(pp, vf[r], o[g][r]);
+          for (int r = 0; r < NPR; ++r) o[g2][r] = ffma2(pp0, vf[r], o[g2][r]);
+          if (g2 + 1 < G) {
+            const float2 pp1 = make_float2(pv2.z, pv2.w);
+#pragma unroll
+            for (int r = 0; r < NPR; ++r) o[g2 + 1][r] = ffma2(pp1, vf[r], o[g2 + 1][r]);
+          }
         }
       }
     }
@@ -722,10 +771,11 @@ cudaError_t plan_decode(const pa_cache_desc& d, int batch, int max_ctx, int max_
   off = pl.off_meta + kStages * 16;
   pl.off_abort = static_cast<uint32_t>(off);
   off += 16;
-  pl.p_row = G <= 4 ? 4 : 8;
+  pl.p_row = p_row_floats(G);
   pl.off_p = static_cast<uint32_t>(align_up(off, 16));
   off = pl.off_p + static_cast<size_t>(pl.nw) * pl.tokens_per_chunk * pl.p_row * 4;
-  pl.off_alpha = static_cast<uint32_t>(off);
+  pl.off_alpha = static_cast<uint32_t>(align_up(off, 16));
+  off = pl.off_alpha;
   off += static_cast<size_t>(pl.nw) * 8 * 4;
   pl.off_ml = static_cast<uint32_t>(off);
   off += static_cast<size_t>(pl.nw) * 16 * 4;
