@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
   const int T = 1 << p.log2T;
   const int cap = static_cast<int>(min(static_cast<int64_t>(p.max_ctx), static_cast<int64_t>(p.maxp) << p.log2P));
   if (tid == 0) carry = 0;
-  __syncthreads();
+  cta_sync();
   for (int base = 0; base < p.B; base += kPlanThreads) {
     const int b = base + tid;
     int cnt = 0;
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
       if ((tid & 31) >= o) x += y;
     }
     if ((tid & 31) == 31) warp_tot[tid >> 5] = x;
-    __syncthreads();
+    cta_sync();
     if (tid < 32) {
       int w = warp_tot[tid];
 #pragma unroll
@@ -123,15 +123,15 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
       }
       warp_tot[tid] = w;
     }
-    __syncthreads();
+    cta_sync();
     const int incl = x + ((tid >> 5) ? warp_tot[(tid >> 5) - 1] : 0) + carry;
     if (b < p.B) p.cs[b + 1] = incl;
-    __syncthreads();
+    cta_sync();
     if (tid == kPlanThreads - 1) carry = incl;
-    __syncthreads();
+    cta_sync();
   }
   if (tid == 0) p.cs[0] = 0;
-  __syncthreads();
+  cta_sync();
   const int NC = carry;
   for (int c = tid; c < p.n_ctas; c += kPlanThreads) {
     const int64_t x0 = (static_cast<int64_t>(c) * NC) / p.n_ctas;
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  cta_sync();
 
   if (warp == NW) {
     // ------------------------------ producer ------------------------------
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const KPara
 #pragma unroll
     for (int e = 0; e < EL; ++e) red[warp][lane][e] = acc[e];
     red[warp][lane][EL] = wsum;
-    __syncthreads();
+    cta_sync();
     if (sub != 0) return;
     for (int w2 = 1; w2 < W; ++w2) {
 #pragma unroll

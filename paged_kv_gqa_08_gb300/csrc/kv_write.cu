@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(128) norm_rope_kv_write_kernel(const NormRopeP
     cs_s[threadIdx.x] = cv;
     sn_s[threadIdx.x] = sv;
   }
-  __syncthreads();
+  cta_sync();
   float cs[PE], sn[PE];
 #pragma unroll
   for (int e = 0; e < PE; ++e) {

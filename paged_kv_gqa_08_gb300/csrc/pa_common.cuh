@@ -135,6 +135,17 @@ PA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 PA_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ----------------------------------------------------------------------------
+// CTA barrier entered by whole warps.  bar.sync (what __syncthreads emits)
+// must be executed by all threads of a warp together; a warp whose lanes took
+// different paths (one lane issuing MMAs or copies while the others skip
+// ahead) reconverges first.
+// ----------------------------------------------------------------------------
+PA_DEVINL void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
+// ----------------------------------------------------------------------------
 // named barriers (subset of warps)
 // ----------------------------------------------------------------------------
 PA_DEVINL void named_bar_sync(int id, int nthreads) {

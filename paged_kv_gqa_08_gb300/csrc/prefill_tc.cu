@@ -11,8 +11,9 @@
 // TQ = 128 / G tokens x the G q-heads that share the kv-head, so each staged
 // K/V tile feeds the whole GQA group, and it feeds both q-tiles of the pair
 // (256 rows per K/V tile).
-//   warp 0     TMA producer of Q and K: both Q tiles once (3-D map), then per
-//              128-key tile the K rows gathered page by page with 16-row boxes
+//   warp 0     TMA producer of Q and K: both Q tiles once (3-D map) and K
+//              tile 0 go out during the CTA's setup, then per 128-key tile
+//              the K rows gathered page by page with 16-row boxes
 //              (single-row boxes for a ragged end, so no slot past the context
 //              is read); block-table entries are read one tile ahead.
 //   warp 10    TMA producer of V, the same way; K and V run ahead of the MMAs
@@ -295,13 +296,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16) + 1;
 
-  // Rows never loaded must hold finite values: zero both Q tiles and both V stages.
+  // Producer lane geometry.  Block-table entries are read one tile ahead: the
+  // loads for tile j + 1 are issued before tile j's stage waits, so their
+  // latency is hidden behind them; tile 0's are read before the setup below.
+  // kNoPage marks an entry the lane does not need.
+  const bool producer = warp == 0 || warp == kVWarp;
+  const bool vrole = warp == kVWarp;
+  const int64_t bt_row = static_cast<int64_t>(b) * p.maxp;
+  const int box = lane >> 2, half = (lane >> 1) & 1, isv = lane & 1;
+  const int x = h * 128 + half * 64;
+  constexpr int kNoPage = INT_MIN;
+  auto load_pages = [&](int jj, int& pg_full, int& pg_rem) {
+    const int t0 = (j_lo + jj) * kBN;
+    const int valid = min(kBN, kv_len - t0);
+    const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+    pg_full = box < nfull ? p.bt[bt_row + ((t0 + box * kBoxRows) >> p.log2P)] : kNoPage;
+    pg_rem = rem && lane < 4 ? p.bt[bt_row + ((t0 + nfull * kBoxRows) >> p.log2P)] : kNoPage;
+  };
+  int pf_next = kNoPage, pr_next = kNoPage;
+  if (producer) load_pages(0, pf_next, pr_next);
+
+  // V rows past the last key are never loaded but meet a probability of 0 in
+  // the PV products, so they must hold finite values: zero both V stages.  Q
+  // needs nothing (and is loaded during this setup): a q-tile in use is always
+  // a whole TMA box, and an unused one is never read.
   {
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads) {
-      reinterpret_cast<uint4*>(smem + kOffQ)[i] = z;
+    for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads)
       reinterpret_cast<uint4*>(smem + kOffV)[i] = z;
-    }
   }
   fence_async_smem();
   if (threadIdx.x == 0) {
@@ -318,6 +340,64 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     mbar_init(o_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // both Q tiles, issued before the setup barrier so that their latency overlaps it
+    mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nq * 2 * p.G * p.TQ * 128));
+    for (int g = 0; g < nq; ++g) {
+      const int z = s0 + (2 * qp + g) * p.TQ;
+      tma_load_3d(smem + kOffQ + g * kTileBytes, &p.tm_q, 0, h * p.G, z, q_full);
+      tma_load_3d(smem + kOffQ + g * kTileBytes + kHalfBytes, &p.tm_q, 64, h * p.G, z, q_full);
+    }
+  }
+
+  // One K or V tile (by the role of the calling producer warp): page ids ->
+  // rows of the cache, the stage's byte count, then one TMA box per lane.
+  // False when the stage wait ran out.
+  auto issue_tile = [&](int j, int pf, int pr) -> bool {
+    const int st = j & 1;
+    const uint32_t par = ((j >> 1) & 1) ^ 1;
+    const int t0 = (j_lo + j) * kBN;
+    const int valid = min(kBN, kv_len - t0);
+    const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+    int y_full = -1, y_rem = -1;
+    if (pf != kNoPage) {
+      const int key0 = t0 + box * kBoxRows;
+      if (pf >= 0 && pf < p.num_pages) y_full = (pf << p.log2P) + (key0 & (p.P - 1));
+      else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
+    }
+    if (pr != kNoPage) {
+      const int key0 = t0 + nfull * kBoxRows;
+      if (pr >= 0 && pr < p.num_pages) y_rem = (pr << p.log2P) + (key0 & (p.P - 1));
+      else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
+    }
+    uint32_t mine = (y_full >= 0 ? kBoxRows * 128 : 0) + (y_rem >= 0 ? rem * 128 : 0);
+    uint32_t bytes = (isv != 0) == vrole ? mine : 0;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+    uint64_t* full = vrole ? &v_full[st] : &k_full[st];
+    int okw = 1;
+    if (lane == 0) {
+      okw = mbar_wait_bounded(vrole ? &v_empty[st] : &k_empty[st], par, abort_flag, p.err);
+      if (okw) mbar_arrive_expect_tx(full, bytes);
+    }
+    if (__shfl_sync(0xffffffffu, okw, 0) == 0) return false;
+    if ((isv != 0) == vrole) {
+      unsigned char* dst = smem + (vrole ? kOffV : kOffK) + st * kTileBytes + half * kHalfBytes;
+      const CUtensorMap* m16 = vrole ? &p.tm_v16 : &p.tm_k16;
+      const CUtensorMap* m1 = vrole ? &p.tm_v1 : &p.tm_k1;
+      if (y_full >= 0) tma_load_2d(dst + box * kBoxRows * 128, m16, x, y_full, full);
+      if (y_rem >= 0)
+        for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, m1, x, y_rem + r, full);
+    }
+    return true;
+  };
+  // K tile 0 goes out before the setup barrier as well (the K region is not
+  // zeroed, and a stage's first wait passes at once)
+  int k_first = 0;
+  if (warp == 0) {
+    __syncwarp();  // lane 0's barrier initialisation is visible to the warp
+    const int pf = pf_next, pr = pr_next;
+    if (nt > 1) load_pages(1, pf_next, pr_next);
+    if (issue_tile(0, pf, pr)) k_first = 1;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -326,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -334,95 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // ------------------------------- TMA producers -------------------------------
     // warp 0 copies Q and the K tiles, warp kVWarp the V tiles; each runs ahead
     // as far as its own stages allow
-    const bool vrole = warp == kVWarp;
-    int issued_k = 0, issued_v = 0;
-    bool ok = true;
-    if (lane == 0 && !vrole) {
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nq * 2 * p.G * p.TQ * 128));
-      for (int g = 0; g < nq; ++g) {
-        const int z = s0 + (2 * qp + g) * p.TQ;
-        tma_load_3d(smem + kOffQ + g * kTileBytes, &p.tm_q, 0, h * p.G, z, q_full);
-        tma_load_3d(smem + kOffQ + g * kTileBytes + kHalfBytes, &p.tm_q, 64, h * p.G, z, q_full);
-      }
-    }
-    const int64_t bt_row = static_cast<int64_t>(b) * p.maxp;
-    const int box = lane >> 2, half = (lane >> 1) & 1, isv = lane & 1;
-    const int x = h * 128 + half * 64;
-    // Block-table entries are read one tile ahead: the loads for tile j + 1
-    // are issued before tile j's stage waits, so their latency is hidden
-    // behind them.  kNoPage marks an entry the lane does not need.
-    constexpr int kNoPage = INT_MIN;
-    auto load_pages = [&](int jj, int& pg_full, int& pg_rem) {
-      const int t0 = (j_lo + jj) * kBN;
-      const int valid = min(kBN, kv_len - t0);
-      const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
-      pg_full = box < nfull ? p.bt[bt_row + ((t0 + box * kBoxRows) >> p.log2P)] : kNoPage;
-      pg_rem = rem && lane < 4 ? p.bt[bt_row + ((t0 + nfull * kBoxRows) >> p.log2P)] : kNoPage;
-    };
-    int pf_next = kNoPage, pr_next = kNoPage;
-    if (nt > 0) load_pages(0, pf_next, pr_next);
-    for (int j = 0; j < nt && ok; ++j) {
-      const int st = j & 1;
-      const uint32_t par = ((j >> 1) & 1) ^ 1;
-      const int t0 = (j_lo + j) * kBN;
-      const int valid = min(kBN, kv_len - t0);
-      const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+    int issued = vrole ? 0 : k_first;
+    bool ok = vrole || k_first == 1;
+    for (int j = issued; j < nt && ok; ++j) {
       const int pf = pf_next, pr = pr_next;
       if (j + 1 < nt) load_pages(j + 1, pf_next, pr_next);
-      int y_full = -1, y_rem = -1;
-      if (pf != kNoPage) {
-        const int key0 = t0 + box * kBoxRows;
-        if (pf >= 0 && pf < p.num_pages) y_full = (pf << p.log2P) + (key0 & (p.P - 1));
-        else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
-      }
-      if (pr != kNoPage) {
-        const int key0 = t0 + nfull * kBoxRows;
-        if (pr >= 0 && pr < p.num_pages) y_rem = (pr << p.log2P) + (key0 & (p.P - 1));
-        else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
-      }
-      uint32_t mine = (y_full >= 0 ? kBoxRows * 128 : 0) + (y_rem >= 0 ? rem * 128 : 0);
-      uint32_t kb = isv ? 0 : mine, vb = isv ? mine : 0;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        kb += __shfl_xor_sync(0xffffffffu, kb, o);
-        vb += __shfl_xor_sync(0xffffffffu, vb, o);
-      }
-      if (!vrole) {
-      int okk = 1;
-      if (lane == 0) {
-        okk = mbar_wait_bounded(&k_empty[st], par, abort_flag, p.err);
-        if (okk) mbar_arrive_expect_tx(&k_full[st], kb);
-      }
-      ok = __shfl_sync(0xffffffffu, okk, 0) != 0;
-      if (!ok) break;
-      if (!isv) {
-        unsigned char* dst = smem + kOffK + st * kTileBytes + half * kHalfBytes;
-        if (y_full >= 0) tma_load_2d(dst + box * kBoxRows * 128, &p.tm_k16, x, y_full, &k_full[st]);
-        if (y_rem >= 0)
-          for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, &p.tm_k1, x, y_rem + r, &k_full[st]);
-      }
-      ++issued_k;
-      } else {
-      int okv = 1;
-      if (lane == 0) {
-        okv = mbar_wait_bounded(&v_empty[st], par, abort_flag, p.err);
-        if (okv) mbar_arrive_expect_tx(&v_full[st], vb);
-      }
-      ok = __shfl_sync(0xffffffffu, okv, 0) != 0;
-      if (!ok) break;
-      if (isv) {
-        unsigned char* dst = smem + kOffV + st * kTileBytes + half * kHalfBytes;
-        if (y_full >= 0) tma_load_2d(dst + box * kBoxRows * 128, &p.tm_v16, x, y_full, &v_full[st]);
-        if (y_rem >= 0)
-          for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, &p.tm_v1, x, y_rem + r, &v_full[st]);
-      }
-      ++issued_v;
-      }
+      ok = issue_tile(j, pf, pr);
+      if (ok) ++issued;
     }
     if (!ok && lane == 0) {
       if (!vrole) drain(q_full, 0);
-      for (int j = max(0, issued_k - 2); j < issued_k; ++j) drain(&k_full[j & 1], (j >> 1) & 1);
-      for (int j = max(0, issued_v - 2); j < issued_v; ++j) drain(&v_full[j & 1], (j >> 1) & 1);
+      uint64_t* full = vrole ? v_full : k_full;
+      for (int j = max(0, issued - 2); j < issued; ++j) drain(&full[j & 1], (j >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------- MMA issuer -------------------------------
@@ -625,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -683,7 +686,7 @@ PA_DEVINL T block_scan_excl(T v, T* sh, T* total) {
     if (lane >= o) x += y;
   }
   if (lane == 31) sh[warp] = x;
-  __syncthreads();
+  cta_sync();
   if (warp == 0) {
     T w = lane < nw ? sh[lane] : T(0);
 #pragma unroll
@@ -693,10 +696,10 @@ PA_DEVINL T block_scan_excl(T v, T* sh, T* total) {
     }
     sh[lane] = w;
   }
-  __syncthreads();
+  cta_sync();
   const T r = (warp > 0 ? sh[warp - 1] : T(0)) + x - v;
   *total = sh[nw - 1];
-  __syncthreads();
+  cta_sync();
   return r;
 }
 
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     return;
   }
   const int n_pairs = static_cast<int>(carry);
-  __syncthreads();
+  cta_sync();
   max_nt = sh_max_nt;
   auto pair_at = [&](int i) -> int4 { return i < kPlanSmemPairs ? sh_pairs[i] : q.pairs[i]; };
 
@@ -790,7 +793,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
         cand_tau[c] = t_c;
       }
     }
-    __syncthreads();
+    cta_sync();
     if (warp == 0) {
       // arg-min; ties go to the lower index (the larger part size)
       float e = lane < n_cand ? cand_est[lane] : INFINITY;
@@ -806,7 +809,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
       }
       if (lane == 0) sh_tau = e < INFINITY ? cand_tau[c] : max_nt;  // candidate 0 (no split) is always finite
     }
-    __syncthreads();
+    cta_sync();
     tau = sh_tau;
   }
 
@@ -817,7 +820,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     if (rem) atomicAdd(&cursor[min(base + 1, kPlanBuckets - 1)], rem);
     if (parts > rem) atomicAdd(&cursor[min(base, kPlanBuckets - 1)], parts - rem);
   }
-  __syncthreads();
+  cta_sync();
   {
     static_assert(kPlanBuckets == 2 * kPlanThreads, "two buckets per thread");
     const int hi = kPlanBuckets - 1 - 2 * tid, lo = hi - 1;
@@ -826,7 +829,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     const int ex = static_cast<int>(block_scan_excl<unsigned long long>(c_hi + c_lo, sh_scan, &tot));
     cursor[hi] = ex;
     cursor[lo] = ex + c_hi;
-    __syncthreads();
+    cta_sync();
   }
 
   // 4. units, partial slots and the split list; one scan of
