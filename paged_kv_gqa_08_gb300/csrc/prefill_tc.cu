@@ -760,7 +760,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
 
   // 2. the part size: one candidate per warp, from max_nt (no split) down to 2
   int tau = max(max_nt, 1);
-  if (n_pairs > 0 && max_nt > 2 &&
+  if (n_pairs > 0 && max_nt > 2 && q.slot_cap > 1 &&
       static_cast<int64_t>(n_pairs) * q.Hkv <= static_cast<int64_t>(kSplitWaves) * q.n_sm) {
     const int n_cand = min(kPlanCandidates, max_nt - 1);
     if (warp < n_cand) {
@@ -987,7 +987,13 @@ cudaError_t plan_prefill(const pa_cache_desc& d, int32_t batch, int32_t max_seql
   pl.n_sm = di.sm_count;
   pl.pair_cap = static_cast<int32_t>(pair_cap);
   pl.slot_cap = std::min(kMaxSlots, (kSplitWaves * di.sm_count + d.num_kv_heads - 1) / d.num_kv_heads);
-  pl.split_cap = pl.slot_cap / 2;
+  // The planner splits only while the pairs fill at most kSplitWaves waves, and
+  // there are at least num_tokens / (2 TQ) pairs: when those alone fill more,
+  // nothing is split and no merge is launched.  A split pair is one of the
+  // pairs, so at most pair_cap of them; the merge grid is sized by this bound
+  // (its CTAs past the planner's count exit at once, but still cost a launch).
+  if (num_tokens / (2 * TQ) * d.num_kv_heads > static_cast<int64_t>(kSplitWaves) * di.sm_count) pl.slot_cap = 0;
+  pl.split_cap = static_cast<int32_t>(std::min<int64_t>(pl.slot_cap / 2, pair_cap));
   pl.unit_cap = pl.pair_cap + pl.slot_cap;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
