@@ -366,17 +366,29 @@ def flush_l2(buf: torch.Tensor) -> None:
     buf.view(torch.int64).sum()
 
 
-def time_graph_parts(d: Device, steps: int, warmup: int, flush=None):
+def time_graph_parts(d: Device, steps: int, warmup: int, flush=None, warm_s: float = 0.0):
     """The write part and the attention call as two CUDA graphs, L2 flushed
     before every step when `flush` (a buffer larger than L2) is given; CUDA
-    events around each replay.  Returns mean (step, write, attention) ms."""
+    events around each replay.  Warm-up: `warmup` steps, continued until
+    `warm_s` seconds of replays have passed.  Returns mean (step, write,
+    attention) ms."""
     gw = capture_graph(d.write_part)
     ga = capture_graph(d.attn_part)
-    for _ in range(warmup):
+
+    def warm_step():
         if flush is not None:
             flush_l2(flush)
         gw.replay()
         ga.replay()
+
+    for _ in range(warmup):
+        warm_step()
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + warm_s
+    while time.perf_counter() < t_end:
+        for _ in range(10):
+            warm_step()
+        torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     torch.cuda.synchronize()
     for k in range(steps):
@@ -667,13 +679,15 @@ def main():
     # ---------------- secondary: prefill and the other decode shapes ----------------
     if not args.no_extra:
         extra = {"timing": "each config's KV-write part and attention call replayed as two CUDA graphs with CUDA "
-                           "events around each replay; prefill configs (KV fits in L2): L2 flushed before every "
-                           "step (512 MiB overwritten, then read back); decode configs with KV > 512 MiB: no flush"}
+                           "events around each replay, after at least 0.2 s of warm-up replays (the GPU idles "
+                           "while a config's inputs are generated on the host); prefill configs (KV fits in L2): "
+                           "L2 flushed before every step (512 MiB overwritten, then read back); decode configs "
+                           "with KV > 512 MiB: no flush"}
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         for name, steps in (("qwen3_0p6b_chunked_prefill", 100), ("prefill_2k", 20)):
             w = synth.make_workload(name)
             dd = Device(w, dev)
-            step_ms, w_ms, a_ms = time_graph_parts(dd, steps, 5, flush)
+            step_ms, w_ms, a_ms = time_graph_parts(dd, steps, 5, flush, warm_s=0.2)
             fl = prefill_flops(w)
             tflops = fl / (a_ms * 1e-3) / 1e12
             rt = max(fl / (tc_peak * 1e12), prefill_call_bytes(w) / (hbm_peak * 1e9))
@@ -688,7 +702,8 @@ def main():
         for name in ("qwen3_8b_decode", "long_context_decode", "tiny_fp32_decode"):
             w = synth.make_workload(name)
             dd = Device(w, dev)
-            step_ms, w_ms, a_ms = time_graph_parts(dd, 100, 5, None if kv_bytes(w) > (512 << 20) else flush)
+            step_ms, w_ms, a_ms = time_graph_parts(dd, 100, 5, None if kv_bytes(w) > (512 << 20) else flush,
+                                                   warm_s=0.2)
             b = decode_call_bytes(w)
             extra[name] = {"workload": describe(w), "ms_per_step": step_ms, "decode_ms": a_ms, "write_ms": w_ms,
                            "decode_gbs": b / (a_ms * 1e-3) / 1e9, "hbm_frac": b / (a_ms * 1e-3) / 1e9 / hbm_peak,
