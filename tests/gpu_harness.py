@@ -35,7 +35,7 @@ def as_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-class GpuRun:
+class GpuCase:
     """All device state of one workload."""
 
     def __init__(self, wl, device: str = "cuda", max_ctas: int = 0, cache_fill: float = float("nan"),

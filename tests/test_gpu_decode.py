@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64
+from gpu_harness import GpuCase, as_f64
 from paged_kv_gqa_08_gb300 import (PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_PAGE, pa_decode, pa_decode_workspace_size,
                                    pa_read_device_errors)
 
@@ -22,7 +22,7 @@ def _check(out, ref, dtype):
 def test_decode_configs_match_oracle(name):
     wl = synth.make_workload(name)
     pa_read_device_errors(reset=True)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
@@ -52,7 +52,7 @@ def test_decode_small_shapes(case, max_ctas):
     dtype, Hq, Hkv, hd, P, lens = case
     spec = dict(kind="decode", dtype=dtype, B=len(lens), Hq=Hq, Hkv=Hkv, hd=hd, P=P, context_lens=lens, seed=sum(lens))
     wl = synth.make_workload(spec)
-    run = GpuRun(wl, max_ctas=max_ctas)
+    run = GpuCase(wl, max_ctas=max_ctas)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
@@ -65,7 +65,7 @@ def test_decode_split_plans_agree():
     ref = oracle.reference_step(wl)
     outs = []
     for max_ctas in (1, 3, 0):
-        run = GpuRun(wl, max_ctas=max_ctas)
+        run = GpuCase(wl, max_ctas=max_ctas)
         outs.append(run.step().clone())
     torch.cuda.synchronize()
     for o in outs:
@@ -74,7 +74,7 @@ def test_decode_split_plans_agree():
 
 def test_decode_page_permutation_is_bitwise_invariant():
     wl = synth.make_workload("qwen3_0p6b_decode", B=24)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out1 = run.step().clone()
     perm = torch.randperm(wl.num_pages, device="cuda")
     kc2 = torch.empty_like(run.k_cache)
@@ -92,7 +92,7 @@ def test_decode_page_permutation_is_bitwise_invariant():
 def test_decode_flags_bad_metadata_and_keeps_other_requests_right():
     wl = synth.make_workload("qwen3_0p6b_decode", B=6)
     ref = oracle.reference_step(wl)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     run.step()
     torch.cuda.synchronize()
     pa_read_device_errors(reset=True)
@@ -114,7 +114,7 @@ def test_decode_flags_bad_metadata_and_keeps_other_requests_right():
 
 def test_decode_zero_batch_is_a_no_op():
     wl = synth.make_workload("tiny_fp32_decode")
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     pa_decode(run.desc, run.t["q"], 0, run.k_cache, run.v_cache, run.t["block_tables"], wl.max_pages_per_seq,
               run.t["context_lens"], wl.max_context_len, wl.scale, 0, run.bufs.out, run.bufs.workspace)
     torch.cuda.synchronize()
@@ -123,7 +123,7 @@ def test_decode_zero_batch_is_a_no_op():
 def test_decode_workspace_too_small_is_rejected():
     from paged_kv_gqa_08_gb300 import PA_ERR_WORKSPACE, PagedAttnError
     wl = synth.make_workload("tiny_fp32_decode")
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     need = pa_decode_workspace_size(run.desc, wl.batch, wl.max_context_len, 0)
     assert need > 0
     with pytest.raises(PagedAttnError) as e:

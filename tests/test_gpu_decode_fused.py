@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64, storage
+from gpu_harness import GpuCase, as_f64, storage
 from paged_kv_gqa_08_gb300 import PA_DEVERR_BAD_LENGTH, pa_decode_kv_write, pa_read_device_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
@@ -41,7 +41,7 @@ def _check_all(run, wl, out, slots):
 @pytest.mark.parametrize("name", ["tiny_fp32_decode", "qwen3_0p6b_decode", "qwen3_8b_decode", "long_context_decode"])
 def test_fused_decode_configs(name):
     wl = synth.make_workload(name)
-    run = GpuRun(wl)                        # cache holds the history only
+    run = GpuCase(wl)                        # cache holds the history only
     pa_read_device_errors(reset=True)
     out, slots = _fused(run, wl)
     _check_all(run, wl, out, slots)
@@ -62,14 +62,14 @@ def test_fused_decode_small_shapes(case, max_ctas):
     dtype, Hq, Hkv, hd, P, lens = case
     wl = synth.make_workload(dict(kind="decode", dtype=dtype, B=len(lens), Hq=Hq, Hkv=Hkv, hd=hd, P=P,
                                   context_lens=lens, seed=sum(lens) + 5))
-    run = GpuRun(wl, max_ctas=max_ctas)
+    run = GpuCase(wl, max_ctas=max_ctas)
     out, slots = _fused(run, wl, max_ctas)
     _check_all(run, wl, out, slots)
 
 
 def test_fused_decode_reports_skipped_requests():
     wl = synth.make_workload("qwen3_0p6b_decode", B=6)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     pa_read_device_errors(reset=True)
     ctx = run.t["context_lens"].clone()
     ctx[3] = 0

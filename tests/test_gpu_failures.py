@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64
+from gpu_harness import GpuCase, as_f64
 from paged_kv_gqa_08_gb300 import (PA_DEVERR_TIMEOUT, pa_read_device_errors, pa_selftest_bounded_wait,
                                    pa_validate_metadata)
 
@@ -25,7 +25,7 @@ def test_bounded_wait_gives_up_flags_and_leaves_context_usable():
     assert pa_read_device_errors(reset=True) & PA_DEVERR_TIMEOUT
     # the context still runs real work correctly
     wl = synth.make_workload("tiny_fp32_decode")
-    out = GpuRun(wl).step()
+    out = GpuCase(wl).step()
     torch.cuda.synchronize()
     ok, err, bound = oracle.within_tolerance(as_f64(out[: wl.batch]), oracle.reference_step(wl)["o"], wl.dtype)
     assert ok, (err, bound)
@@ -34,7 +34,7 @@ def test_bounded_wait_gives_up_flags_and_leaves_context_usable():
 
 def test_validate_metadata_counts_problems():
     wl = synth.make_workload("qwen3_0p6b_chunked_prefill")
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
     args = (run.desc, wl.batch)
     pa_validate_metadata(*args, run.t["cu_seqlens_q"], run.t["context_lens"], run.t["block_tables"],

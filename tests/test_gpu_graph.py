@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64, storage
+from gpu_harness import GpuCase, as_f64, storage
 from paged_kv_gqa_08_gb300.step import run_step, write_rows
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
@@ -35,7 +35,7 @@ def test_decode_step_replays_from_a_cuda_graph_with_new_inputs():
     spec = dict(synth.CONFIGS["qwen3_0p6b_decode"], B=16, num_pages=2200, max_pages_per_seq=BUCKET_MAX_CTX // 16)
     wl1 = synth.make_workload(spec, seed=101)
     wl2 = synth.make_workload(spec, seed=202)
-    run = GpuRun(wl1)
+    run = GpuCase(wl1)
 
     def step():
         t = run.t
@@ -70,7 +70,7 @@ def test_planned_prefill_step_replays_from_a_cuda_graph_with_new_lengths():
     wl1 = synth.make_workload(dict(base, prefixes=[5000, 20, 300]), seed=11)
     wl2 = synth.make_workload(dict(base, prefixes=[64, 5900, 4000]), seed=12)
     max_ctx = 6000
-    run = GpuRun(wl1)
+    run = GpuCase(wl1)
     assert run.bufs.workspace is not None
 
     def step():

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, storage
+from gpu_harness import GpuCase, storage
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
@@ -39,7 +39,7 @@ def _bits(a: np.ndarray) -> np.ndarray:
 @pytest.mark.parametrize("name", synth.CONFIG_ORDER + ["prefill_2k"])
 def test_step_slot_mapping_and_cache_write(name):
     wl = synth.make_workload(name)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl, with_attention=False)

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64
+from gpu_harness import GpuCase, as_f64
 from paged_kv_gqa_08_gb300 import pa_decode, pa_prefill_varlen, pa_read_device_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
@@ -21,7 +21,7 @@ def _check(out, ref, dtype):
 def test_prefill_configs_match_oracle(name):
     wl = synth.make_workload(name)
     pa_read_device_errors(reset=True)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
@@ -51,7 +51,7 @@ def test_prefill_small_shapes(case):
     spec = dict(kind="prefill", dtype=dtype, B=len(chunks), Hq=Hq, Hkv=Hkv, hd=hd, P=P, chunks=chunks,
                 prefixes=prefixes, norm=norm, seed=sum(chunks) + 7)
     wl = synth.make_workload(spec)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
@@ -61,7 +61,7 @@ def test_prefill_small_shapes(case):
 
 def test_prefill_with_length_one_chunks_matches_decode():
     wl = synth.make_workload("qwen3_0p6b_decode", B=16)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out_dec = run.step().clone()
     out_pf = torch.empty_like(out_dec)
     pa_prefill_varlen(run.desc, run.t["q"], run.t["cu_seqlens_q"], wl.batch, 1, wl.batch, run.k_cache, run.v_cache,
@@ -78,7 +78,7 @@ def test_prefill_empty_requests_in_batch():
     spec = dict(kind="prefill", dtype="bf16", B=4, Hq=16, Hkv=8, hd=128, P=16, chunks=[0, 40, 0, 3],
                 prefixes=[10, 20, 0, 64], norm=True, seed=99)
     wl = synth.make_workload(spec)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
@@ -90,7 +90,7 @@ def test_mixed_decode_rows_and_prefill_chunks_in_one_launch():
     spec = dict(kind="prefill", dtype="bf16", B=6, Hq=32, Hkv=8, hd=128, P=16, chunks=[1, 300, 1, 1, 77, 1],
                 prefixes=[900, 0, 45, 2047, 129, 3], norm=True, seed=21)
     wl = synth.make_workload(spec)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
@@ -106,10 +106,10 @@ def test_planned_and_unplanned_launches_agree_on_the_mixed_chunk_batch():
     wl = synth.make_workload("qwen3_0p6b_chunked_prefill")
     ref = oracle.reference_step(wl)
     pa_read_device_errors(reset=True)
-    plain = GpuRun(wl, plan_prefill=False)
+    plain = GpuCase(wl, plan_prefill=False)
     assert plain.bufs.workspace is None
     out_plain = plain.step().clone()
-    planned = GpuRun(wl)
+    planned = GpuCase(wl)
     out_planned = planned.step()
     torch.cuda.synchronize()
     units, splits, tau, pairs = _plan_header(planned)
@@ -135,7 +135,7 @@ def test_split_key_ranges_match_oracle(case):
                 prefixes=prefixes, norm=True, seed=sum(prefixes) % 1000 + 3)
     wl = synth.make_workload(spec)
     pa_read_device_errors(reset=True)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     units, splits, tau, pairs = _plan_header(run)
@@ -150,7 +150,7 @@ def test_planned_prefill_with_empty_requests_and_tiny_workload():
                 prefixes=[10, 5000, 0, 1, 7], norm=True, seed=5)
     wl = synth.make_workload(spec)
     pa_read_device_errors(reset=True)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     assert _plan_header(run)[3] == 2          # only the two non-empty requests have pairs
@@ -178,7 +178,7 @@ def test_random_planned_batches_match_oracle(seed):
                 prefixes=prefixes, norm=bool(seed % 2), seed=seed + 50)
     wl = synth.make_workload(spec)
     pa_read_device_errors(reset=True)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64
+from gpu_harness import GpuCase, as_f64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
@@ -38,7 +38,7 @@ def test_shared_prefix_pages(kind):
     assert pages >= 2
     _share_prefix(wl, a, b, pages)
     _share_prefix(wl, a, c, pages)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from gpu_harness import GpuRun, as_f64
+from gpu_harness import GpuCase, as_f64
 from paged_kv_gqa_08_gb300 import PA_BF16, PA_ERR_WORKSPACE, PA_OK, cache_desc, load_library, pa_read_device_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
@@ -33,7 +33,7 @@ def _call(lib, run, wl, out, batch=None, max_ctx=None):
 def test_no_alloc_matches_pa_decode_on_two_calls_in_a_row(name):
     lib = load_library()
     wl = synth.make_workload(name)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     ref = as_f64(run.step()[: wl.batch])          # pa_decode with a caller workspace
     pa_read_device_errors(reset=True)
     for _ in range(2):                              # the second call reuses the scratch as the first left it
@@ -48,7 +48,7 @@ def test_no_alloc_matches_pa_decode_on_two_calls_in_a_row(name):
 def test_no_alloc_rejects_a_batch_larger_than_its_scratch():
     lib = load_library()
     wl = synth.make_workload("qwen3_0p6b_decode", B=4)
-    run = GpuRun(wl)
+    run = GpuCase(wl)
     out = torch.empty_like(run.bufs.out)
     # 4096 requests of 64 q-heads x 128 need far more than 16 MiB of partials;
     # the call is refused on the host before anything is enqueued
