@@ -130,11 +130,12 @@ __global__ void __launch_bounds__(128) norm_rope_kv_write_kernel(const NormRopeP
     sn_s[threadIdx.x] = sv;
   }
   cta_sync();
-  float cs[PE], sn[PE];
+  float cs[PE], sn[PE], nsn[PE];
 #pragma unroll
   for (int e = 0; e < PE; ++e) {
     cs[e] = cs_s[l * PE + e];
     sn[e] = sn_s[l * PE + e];
+    nsn[e] = -sn[e];
   }
   float wq_a[PE], wq_b[PE], wk_a[PE], wk_b[PE];
   Vec4<T>::load(static_cast<const T*>(p.wq) + l * PE, wq_a);
@@ -160,22 +161,49 @@ __global__ void __launch_bounds__(128) norm_rope_kv_write_kernel(const NormRopeP
     for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
     if (!active) continue;
     const float r = 1.0f / sqrtf(ss / HD + p.eps);
-    float ya[PE], yb[PE];
+    T* dst = isq ? static_cast<T*>(p.q_out) + (t * p.hq + hh) * HD
+                 : static_cast<T*>(p.k_cache) + (slot * p.hkv + (hh - p.hq)) * HD;
+    const bool store = isq || slot_ok;
+    if constexpr (sizeof(T) == 2) {
+      // pairs of elements in packed fp32 arithmetic; each bf16 rounding is one
+      // two-lane conversion, the last one the store's packing:
+      // y_a = n_a cos - n_b sin, y_b = n_b cos + n_a sin
+      uint32_t wa[PE / 2], wb[PE / 2];
+      const float2 r2 = make_float2(r, r);
 #pragma unroll
-    for (int e = 0; e < PE; ++e) {
-      const float na = round_to<T>(round_to<T>(xa[e] * r) * (isq ? wq_a[e] : wk_a[e]));
-      const float nb = round_to<T>(round_to<T>(xb[e] * r) * (isq ? wq_b[e] : wk_b[e]));
-      ya[e] = round_to<T>(na * cs[e] - nb * sn[e]);
-      yb[e] = round_to<T>(nb * cs[e] + na * sn[e]);
-    }
-    if (isq) {
-      T* dst = static_cast<T*>(p.q_out) + (t * p.hq + hh) * HD;
-      Vec4<T>::store(dst + l * PE, ya);
-      Vec4<T>::store(dst + HD / 2 + l * PE, yb);
-    } else if (slot_ok) {
-      T* dst = static_cast<T*>(p.k_cache) + (slot * p.hkv + (hh - p.hq)) * HD;
-      Vec4<T>::store(dst + l * PE, ya);
-      Vec4<T>::store(dst + HD / 2 + l * PE, yb);
+      for (int e2 = 0; e2 < PE / 2; ++e2) {
+        const int e = 2 * e2;
+        const float2 gwa = isq ? make_float2(wq_a[e], wq_a[e + 1]) : make_float2(wk_a[e], wk_a[e + 1]);
+        const float2 gwb = isq ? make_float2(wq_b[e], wq_b[e + 1]) : make_float2(wk_b[e], wk_b[e + 1]);
+        float2 ta = fmul2(make_float2(xa[e], xa[e + 1]), r2);
+        float2 tb = fmul2(make_float2(xb[e], xb[e + 1]), r2);
+        ta = fmul2(bf16x2_to_float2(pack_bf16x2(ta.x, ta.y)), gwa);
+        tb = fmul2(bf16x2_to_float2(pack_bf16x2(tb.x, tb.y)), gwb);
+        const float2 na = bf16x2_to_float2(pack_bf16x2(ta.x, ta.y));
+        const float2 nb = bf16x2_to_float2(pack_bf16x2(tb.x, tb.y));
+        const float2 c2 = make_float2(cs[e], cs[e + 1]);
+        const float2 ya = ffma2(nb, make_float2(nsn[e], nsn[e + 1]), fmul2(na, c2));
+        const float2 yb = ffma2(nb, c2, fmul2(na, make_float2(sn[e], sn[e + 1])));
+        wa[e2] = pack_bf16x2(ya.x, ya.y);
+        wb[e2] = pack_bf16x2(yb.x, yb.y);
+      }
+      if (store) {
+        *reinterpret_cast<uint2*>(dst + l * PE) = make_uint2(wa[0], wa[1]);
+        *reinterpret_cast<uint2*>(dst + HD / 2 + l * PE) = make_uint2(wb[0], wb[1]);
+      }
+    } else {
+      float ya[PE], yb[PE];
+#pragma unroll
+      for (int e = 0; e < PE; ++e) {
+        const float na = round_to<T>(round_to<T>(xa[e] * r) * (isq ? wq_a[e] : wk_a[e]));
+        const float nb = round_to<T>(round_to<T>(xb[e] * r) * (isq ? wq_b[e] : wk_b[e]));
+        ya[e] = round_to<T>(na * cs[e] - nb * sn[e]);
+        yb[e] = round_to<T>(nb * cs[e] + na * sn[e]);
+      }
+      if (store) {
+        Vec4<T>::store(dst + l * PE, ya);
+        Vec4<T>::store(dst + HD / 2 + l * PE, yb);
+      }
     }
   }
   if (slot_ok) {
