@@ -71,7 +71,11 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
 // fused q/k RMSNorm + rotary + KV scatter.  One CTA (4 warps) per token.
 // A group of LPH lanes handles one head: lane l owns elements
 // [4l, 4l+4) of the first half and the same of the second half, so each lane
-// holds both members of its rotation pairs.
+// holds both members of its rotation pairs.  Values are rounded to the storage
+// type after the normalisation, after the weight and after the rotation (the
+// casts of the Qwen3 norm and rotary in the nano-vLLM learning note); for bf16
+// the element arithmetic runs on fp32 pairs (packed multiplies and FMAs, one
+// two-lane conversion per rounding).
 // ---------------------------------------------------------------------------
 template <typename T>
 struct Vec4;
