@@ -43,6 +43,11 @@ SMALL = [
     ("bf16", 4, 4, 64, 16, [9, 200, 31]),           # G = 1, head_dim 64
     ("bf16", 16, 2, 64, 128, [1, 1000]),            # G = 8, head_dim 64
     ("bf16", 2, 1, 128, 16, [50, 51]),              # one kv head
+    ("bf16", 48, 8, 128, 16, [300, 45, 1]),         # G = 6 (heads padded to 8 in the reduction)
+    ("bf16", 28, 4, 128, 32, [130, 7]),             # G = 7
+    ("bf16", 12, 2, 64, 16, [66, 500]),             # G = 6, head_dim 64
+    ("f32", 14, 2, 64, 16, [20, 90]),               # G = 7
+    ("f32", 24, 4, 128, 16, [64, 3]),               # G = 6, head_dim 128
 ]
 
 

@@ -53,6 +53,8 @@ SMALL = [
     ("bf16", 24, 8, 128, 16, [1, 2, 77, 500]),
     ("bf16", 32, 4, 128, 256, [255, 256, 257, 3000]),
     ("bf16", 4, 4, 64, 16, [9, 200, 31]),
+    ("bf16", 48, 8, 128, 16, [300, 45, 1]),         # G = 6
+    ("bf16", 28, 4, 128, 32, [130, 7]),             # G = 7
 ]
 
 
