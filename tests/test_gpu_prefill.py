@@ -38,6 +38,8 @@ SMALL = [
     ("bf16", 32, 4, 128, 16, [17, 40], [160, 2], False),        # G = 8
     ("bf16", 24, 8, 128, 16, [45, 12], [9, 130], True),         # G = 3
     ("bf16", 20, 4, 128, 64, [30, 26], [64, 1], False),         # G = 5
+    ("bf16", 48, 8, 128, 16, [40, 9], [100, 0], True),          # G = 6 (21-token q-tiles, 126 rows)
+    ("bf16", 28, 4, 128, 32, [25, 70], [5, 200], False),        # G = 7 (18-token q-tiles)
     ("bf16", 8, 4, 64, 16, [20, 5], [40, 0], True),             # head_dim 64 (CUDA-core kernel)
     ("f32", 4, 2, 64, 16, [1, 9, 33], [0, 16, 5], True),
     ("f32", 8, 4, 128, 32, [70, 2], [0, 100], False),
