@@ -23,9 +23,7 @@ import argparse
 import ctypes
 import hashlib
 import json
-import math
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -39,7 +37,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 from paged_kv_gqa_08_gb300 import PA_BF16, PA_F32, build as pa_build, cache_desc, load_library  # noqa: E402
 from paged_kv_gqa_08_gb300 import pa_decode, pa_prefill_varlen, pa_read_device_errors  # noqa: E402
-from paged_kv_gqa_08_gb300.step import alloc_step_buffers, run_step, write_rows  # noqa: E402
+from paged_kv_gqa_08_gb300.step import alloc_step_buffers, write_rows  # noqa: E402
 
 METRIC = "paged GQA decode HBM GB/s (% of peak) & attn tok/s; prefill TFLOP/s vs peak"
 UNIT = "GB/s"

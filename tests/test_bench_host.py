@@ -3,9 +3,7 @@ multi-rank aggregation (world size 2 over gloo on the CPU)."""
 import os
 import socket
 
-import numpy as np
 import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

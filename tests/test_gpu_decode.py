@@ -1,5 +1,4 @@
 """GPU parity of batched GQA decode (split-KV + LSE merge) against the oracle."""
-import numpy as np
 import pytest
 import torch
 

@@ -2,7 +2,6 @@
 the metadata validator, and host-side argument errors."""
 import time
 
-import numpy as np
 import pytest
 import torch
 

@@ -3,13 +3,12 @@ allocation inside the calls.  A graph captured once for a batch-size bucket
 replays correctly after the batch's q, new K/V, lengths and block tables are
 replaced in place (qwen-engine README: decode batches captured per padded size
 and replayed with fresh inputs)."""
-import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from gpu_harness import GpuCase, as_f64, storage
+from gpu_harness import GpuCase, as_f64
 from paged_kv_gqa_08_gb300.step import run_step, write_rows
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]

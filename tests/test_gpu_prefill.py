@@ -6,7 +6,7 @@ import torch
 import oracle
 import synth
 from gpu_harness import GpuCase, as_f64
-from paged_kv_gqa_08_gb300 import pa_decode, pa_prefill_varlen, pa_read_device_errors
+from paged_kv_gqa_08_gb300 import pa_prefill_varlen, pa_read_device_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 

@@ -15,7 +15,6 @@ import pytest
 
 import oracle
 import synth
-from oracle import paged_attention as pa
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
