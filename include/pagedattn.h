@@ -295,8 +295,7 @@ PA_API pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, con
  * pa_prefill_workspace_size -- bytes of the optional pa_prefill_varlen
  * workspace for these bounds on the current device (it holds the work list
  * and, for split ranges, fp32 partial outputs of at most 4 waves of CTAs:
- * about 80 MiB on a 152-SM GPU; a few KB when num_tokens alone fills more
- * than 4 waves of q-tile pairs, as nothing is split then), or 0 when the call would not use one
+ * about 80 MiB on a 152-SM GPU), or 0 when the call would not use one
  * (fp32 or head_dim 64, max_context_len beyond 65535 * 128) or the
  * arguments are invalid.
  */

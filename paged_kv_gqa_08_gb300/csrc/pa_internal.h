@@ -158,7 +158,8 @@ struct PrefillArgs {
 // Workspace layout of the planned tensor-core prefill (byte offsets, each
 // 256-aligned); ws_bytes == 0 when the call cannot be planned.
 struct PrefillPlan {
-  int32_t pair_cap, slot_cap, unit_cap, split_cap, n_sm;
+  int32_t pair_cap, slot_cap, unit_cap, split_cap, n_sm;  // workspace layout capacities
+  int32_t run_slot_cap, run_split_cap;  // this call: part slots the planner may use, split pairs it may form
   size_t off_hdr, off_pairs, off_units, off_splits, off_lse, off_o, ws_bytes;
 };
 cudaError_t plan_prefill(const pa_cache_desc& d, int32_t batch, int32_t max_seqlen_q, int64_t num_tokens,

@@ -986,15 +986,20 @@ cudaError_t plan_prefill(const pa_cache_desc& d, int32_t batch, int32_t max_seql
   PrefillPlan& pl = *out;
   pl.n_sm = di.sm_count;
   pl.pair_cap = static_cast<int32_t>(pair_cap);
+  // Layout capacities: they grow with the bounds only, so a workspace sized
+  // for the largest call serves every smaller one.
   pl.slot_cap = std::min(kMaxSlots, (kSplitWaves * di.sm_count + d.num_kv_heads - 1) / d.num_kv_heads);
-  // The planner splits only while the pairs fill at most kSplitWaves waves, and
-  // there are at least num_tokens / (2 TQ) pairs: when those alone fill more,
-  // nothing is split and no merge is launched.  A split pair is one of the
-  // pairs, so at most pair_cap of them; the merge grid is sized by this bound
-  // (its CTAs past the planner's count exit at once, but still cost a launch).
-  if (num_tokens / (2 * TQ) * d.num_kv_heads > static_cast<int64_t>(kSplitWaves) * di.sm_count) pl.slot_cap = 0;
-  pl.split_cap = static_cast<int32_t>(std::min<int64_t>(pl.slot_cap / 2, pair_cap));
+  pl.split_cap = pl.slot_cap / 2;
   pl.unit_cap = pl.pair_cap + pl.slot_cap;
+  // This call: the planner splits only while the pairs fill at most
+  // kSplitWaves waves, and there are at least num_tokens / (2 TQ) pairs, so
+  // when those alone fill more nothing is split and no merge is launched.  A
+  // split pair is one of the pairs, so at most pair_cap of them: the merge grid
+  // is sized by that bound too (its CTAs past the planner's count exit at once,
+  // but still cost a launch).
+  const bool no_split = num_tokens / (2 * TQ) * d.num_kv_heads > static_cast<int64_t>(kSplitWaves) * di.sm_count;
+  pl.run_slot_cap = no_split ? 0 : pl.slot_cap;
+  pl.run_split_cap = no_split ? 0 : static_cast<int32_t>(std::min<int64_t>(pl.split_cap, pair_cap));
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   pl.off_hdr = off;
@@ -1103,8 +1108,8 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   q.max_seqlen_q = a.max_seqlen_q;
   q.cap_ctx = static_cast<int32_t>(std::min<int64_t>(a.max_context_len, int64_t(a.max_pages) << p.log2P));
   q.pair_cap = pl.pair_cap;
-  q.slot_cap = pl.slot_cap;
-  q.split_cap = pl.split_cap;
+  q.slot_cap = pl.run_slot_cap;
+  q.split_cap = pl.run_split_cap;
   prefill_plan_kernel<<<1, kPlanThreads, 0, s>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -1115,12 +1120,13 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   {
     void* args[] = {&p};
     e = launch_after_previous(reinterpret_cast<const void*>(prefill_tc_kernel),
-                              dim3(static_cast<unsigned>(pl.unit_cap) * d.num_kv_heads), dim3(kThreads), kSmemBytes, s,
+                              dim3(static_cast<unsigned>(pl.pair_cap + pl.run_slot_cap) * d.num_kv_heads),
+                              dim3(kThreads), kSmemBytes, s,
                               args);
     if (e != cudaSuccess) return e;
   }
 
-  if (pl.split_cap > 0) {
+  if (pl.run_split_cap > 0) {
     MergeParams m;
     m.cu = a.cu_seqlens_q;
     m.splits = q.splits;
@@ -1134,7 +1140,8 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
     m.TQ = TQ;
     void* args[] = {&m};
     e = launch_after_previous(reinterpret_cast<const void*>(prefill_merge_kernel),
-                              dim3(pl.split_cap * kMergeRowBlocks, d.num_kv_heads), dim3(kMergeThreads), 0, s, args);
+                              dim3(pl.run_split_cap * kMergeRowBlocks, d.num_kv_heads), dim3(kMergeThreads), 0, s,
+                              args);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
