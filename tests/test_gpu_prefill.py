@@ -6,7 +6,7 @@ import torch
 import oracle
 import synth
 from gpu_harness import GpuCase, as_f64
-from paged_kv_gqa_08_gb300 import pa_prefill_varlen, pa_read_device_errors
+from paged_kv_gqa_08_gb300 import pa_prefill_varlen, pa_prefill_workspace_size, pa_read_device_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
@@ -22,6 +22,23 @@ def test_prefill_configs_match_oracle(name):
     wl = synth.make_workload(name)
     pa_read_device_errors(reset=True)
     run = GpuCase(wl)
+    out = run.step()
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
+    assert pa_read_device_errors(reset=True) == 0
+
+
+def test_workspace_sized_for_the_largest_batch_serves_a_smaller_call():
+    """The planned-prefill workspace size never shrinks as the token bound
+    grows, so one workspace sized for the largest batch (here 16k tokens, a
+    batch that would not split) serves the mixed chunked-prefill step."""
+    wl = synth.make_workload("qwen3_0p6b_chunked_prefill")
+    run = GpuCase(wl)
+    sizes = [pa_prefill_workspace_size(run.desc, wl.batch, 2048, n, 8192) for n in (64, 1218, 4096, 16384)]
+    assert sizes[0] > 0 and all(a <= b for a, b in zip(sizes, sizes[1:])), sizes
+    run.bufs.workspace = torch.empty(sizes[-1], dtype=torch.uint8, device="cuda")
+    pa_read_device_errors(reset=True)
     out = run.step()
     torch.cuda.synchronize()
     ref = oracle.reference_step(wl)
