@@ -228,16 +228,16 @@ PA_API pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, co
  * memory.  The pages have no counterpart of this call.
  *
  * For code that cannot call cudaMalloc where it runs decode (a plugin handed
- * only its buffers, a framework that forbids allocations while it builds a CUDA
- * graph, a process whose memory manager owns the device heap).  Arguments and
+ * only its buffers, a framework that forbids allocations at that point, a
+ * process whose memory manager owns the device heap).  Arguments and
  * results are pa_decode's, without the workspace: the split-KV scratch comes
  * from a 16 MiB array inside the library that every device loading the
  * library holds until the process exits.  The call allocates nothing.
  *   - A batch whose plan needs more than 16 MiB of scratch (see
  *     pa_decode_workspace_size) is rejected with PA_ERR_WORKSPACE before
  *     anything is enqueued.
- *   - The first call on a device looks up the array's device address (once per
- *     device); make that first call before any stream capture.
+ *   - The first call on a device looks up the array's device address with a
+ *     host-side runtime query (once per device).
  *   - Every call shares the array and it keeps the last call's contents;
  *     nothing in it has to start at zero, but calls that overlap on the GPU
  *     (two streams, two host threads) race on it.

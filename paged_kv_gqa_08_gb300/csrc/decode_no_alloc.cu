@@ -3,9 +3,8 @@
 //
 // Some callers cannot call cudaMalloc (or any allocating routine) at the point
 // where they run decode: a plugin or embedding that is handed only its input
-// and output buffers, code running while a CUDA graph is being built by a
-// framework that forbids allocations in that window, or a process whose
-// memory manager owns the whole device heap.  pa_decode needs a caller-owned
+// and output buffers, code inside a framework that forbids allocations at that
+// point, or a process whose memory manager owns the whole device heap.  pa_decode needs a caller-owned
 // workspace for its split-KV partials; this variant takes that scratch from a
 // fixed array inside the library instead.  The caller still passes q, the
 // caches, the metadata and the output.

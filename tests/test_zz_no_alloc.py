@@ -1,7 +1,7 @@
 """pa_decode_no_alloc, the decode entry point for callers that cannot
 allocate device memory (a plugin handed only its buffers, a framework that
-forbids allocation while it builds a graph, a process whose allocator owns the
-device heap).  It must give pa_decode's results from the library's fixed
+forbids allocation at that point, a process whose allocator owns the device
+heap).  It must give pa_decode's results from the library's fixed
 scratch, call after call, and refuse batches too large for that scratch.
 
 This file is collected last so that a run stopping at the first failure has
