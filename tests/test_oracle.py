@@ -170,6 +170,53 @@ def test_rope_invariants():
     assert abs(d1 - d2) < 1e-9
 
 
+def test_qk_norm_rope_golden(golden_dir):
+    # Hand-worked q and k of two tokens at positions 1 and 2 with different
+    # q and k norm weights: the weights, the positions and each bf16 cast
+    # (after x*r, after the weight, after the rotation) all move some output.
+    g = _load(golden_dir, "qk_norm_rope_worked.json")
+    bf = lambda a: oracle.narrow(np.array(a, dtype=np.float64), "bf16")
+    qo, ko = oracle.qk_norm_rope(bf(g["q"]), bf(g["k"]), bf(g["q_norm_w"]), bf(g["k_norm_w"]),
+                                 np.array(g["positions"]), g["eps"], g["theta"], g["dtype"])
+    assert oracle.widen(qo, "bf16").tolist() == g["q_out"]
+    assert oracle.widen(ko, "bf16").tolist() == g["k_out"]
+
+
+def test_qk_norm_rope_rows_are_independent_tokens():
+    # A token of a chunk gives the same bits as that token alone at its
+    # position, and every head of a token uses the one weight vector.
+    rng = np.random.default_rng(5)
+    n, Hq, Hkv, hd = 6, 4, 2, 16
+    q = oracle.narrow(rng.standard_normal((n, Hq, hd)), "bf16")
+    k = oracle.narrow(rng.standard_normal((n, Hkv, hd)), "bf16")
+    wq = oracle.narrow(1 + 0.1 * rng.standard_normal(hd), "bf16")
+    wk = oracle.narrow(1 + 0.1 * rng.standard_normal(hd), "bf16")
+    pos = np.array([0, 1, 2, 37, 38, 4095])
+    qo, ko = oracle.qk_norm_rope(q, k, wq, wk, pos, 1e-6, 1e6, "bf16")
+    for t in range(n):
+        q1, k1 = oracle.qk_norm_rope(q[t:t + 1], k[t:t + 1], wq, wk, pos[t:t + 1], 1e-6, 1e6, "bf16")
+        assert np.array_equal(q1[0], qo[t]) and np.array_equal(k1[0], ko[t])
+        for h in range(Hq):
+            qh, _ = oracle.qk_norm_rope(q[t:t + 1, h:h + 1], k[t:t + 1, :1], wq, wk, pos[t:t + 1],
+                                        1e-6, 1e6, "bf16")
+            assert np.array_equal(qh[0, 0], qo[t, h])
+
+
+def test_reference_step_rotates_new_tokens_at_their_positions():
+    # The step's new tokens sit after each request's cached prefix: token j of
+    # a chunk after c cached tokens is rotated at position c + j.
+    chunks, prefixes = [1, 3, 2], [0, 9, 16]
+    wl = synth.make_workload("qwen3_0p6b_chunked_prefill", chunks=chunks, prefixes=prefixes, B=3)
+    r = oracle.reference_step(wl, with_attention=False)
+    t = 0
+    for b in range(3):
+        for j in range(chunks[b]):
+            q1, k1 = oracle.qk_norm_rope(wl.q[t:t + 1], wl.k_new[t:t + 1], wl.q_norm_w, wl.k_norm_w,
+                                         np.array([prefixes[b] + j]), wl.eps, wl.rope_theta, "bf16")
+            assert np.array_equal(r["q"][t], q1[0]) and np.array_equal(r["k"][t], k1[0])
+            t += 1
+
+
 # ---------------------------------------------------------------------------
 # attention
 # ---------------------------------------------------------------------------
