@@ -18,6 +18,14 @@
  * Query-head grouping (nano-vLLM learning note, Qwen3Attention.forward
  * listing): q-head h reads kv-head h / (num_q_heads / num_kv_heads).
  *
+ * Padding rows: a request with context_lens[b] == 0 is padding (a batch
+ * padded up to a fixed size, whose rows past the live requests keep the zero
+ * lengths of buffers created zeroed: nano-vLLM learning note,
+ * ModelRunner.capture_cudagraph listing).  Every call skips it silently: its
+ * new tokens get position 0 and slot -1, nothing is read or stored for it,
+ * its output rows are left untouched, and no PA_DEVERR_* flag is raised.
+ * Negative lengths and lengths beyond the bounds stay errors.
+ *
  * Supported: dtype fp32 or bf16; head_dim 64 or 128; num_kv_heads a power of
  * two <= 8; group size num_q_heads / num_kv_heads in 1..8; page_size a power
  * of two >= 16.  All vector pointers and row strides must be 16-byte aligned.
@@ -90,7 +98,8 @@ typedef void* pa_stream_t;
  *   num_tokens       cu[B] (host).
  *   positions        int32 [num_tokens] out: context_lens[b] - n_b + j.
  *   slot_mapping     int64 [num_tokens] out; -1 (and PA_DEVERR_* raised) for a
- *                    token whose page entry is out of range.
+ *                    token whose page entry is out of range; -1 (no flag) for
+ *                    the tokens of a padding row (context_lens[b] == 0).
  */
 PA_API pa_status pa_slot_mapping(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
                           const int32_t* context_lens, const int32_t* block_tables,
@@ -180,9 +189,10 @@ PA_API pa_status pa_decode_plan_info(const pa_cache_desc* desc, int32_t batch, i
  *
  *   q                [batch, num_q_heads, head_dim] contiguous.
  *   block_tables     int32 [batch, max_pages_per_seq].
- *   context_lens     int32 [batch], each in [1, max_context_len]; a request
- *                    outside that range is skipped (its output untouched) and
- *                    flagged PA_DEVERR_BAD_LENGTH.
+ *   context_lens     int32 [batch], each in [1, max_context_len], or 0 for a
+ *                    padding row (skipped silently, output untouched); a
+ *                    request outside that range is skipped (its output
+ *                    untouched) and flagged PA_DEVERR_BAD_LENGTH.
  *   max_context_len  host upper bound on context_lens (sizes the split plan).
  *   scale            softmax scale (host), e.g. 1/sqrt(head_dim).
  *   max_ctas         0 = library choice; else at most this many partitions
@@ -211,7 +221,8 @@ PA_API pa_status pa_decode(const pa_cache_desc* desc, const void* q, int32_t bat
  *   k_new, v_new     [batch, num_kv_heads, head_dim] rows at k_row_stride /
  *                    v_row_stride (elements, 16-byte multiples).
  *   slot_mapping     optional int64 [batch] out: the slot written for each
- *                    request, -1 for a request skipped for bad metadata.
+ *                    request, -1 for a padding row (context_lens[b] == 0:
+ *                    nothing stored) or a request skipped for bad metadata.
  *   other arguments  as pa_decode; the workspace size is pa_decode's.
  * Needs num_pages * page_size < 2^31 (else PA_ERR_UNSUPPORTED).
  */
@@ -237,7 +248,11 @@ PA_API pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, co
  *     pa_decode_workspace_size) is rejected with PA_ERR_WORKSPACE before
  *     anything is enqueued.
  *   - The first call on a device looks up the array's device address with a
- *     host-side runtime query (once per device).
+ *     host-side runtime query (once per device).  With lazy module loading
+ *     (CUDA_MODULE_LOADING=LAZY, the CUDA runtime's default) that lookup is
+ *     also when the array is placed in the device's memory, so make the first
+ *     call early -- before the caller's memory manager takes the rest of the
+ *     heap, and before any stream capture.  Later calls allocate nothing.
  *   - Every call shares the array and it keeps the last call's contents;
  *     nothing in it has to start at zero, but calls that overlap on the GPU
  *     (two streams, two host threads) race on it.
@@ -263,7 +278,8 @@ PA_API pa_status pa_decode_no_alloc(const pa_cache_desc* desc, const void* q, in
  *                    normed and rotated, e.g. q_out of pa_qk_norm_rope_kv_write).
  *   cu_seqlens_q     int32 [batch+1] as in pa_slot_mapping; num_tokens = cu[batch].
  *   max_seqlen_q     host upper bound on n_b.
- *   context_lens     int32 [batch], n_b <= context_lens[b] <= max_context_len.
+ *   context_lens     int32 [batch], n_b <= context_lens[b] <= max_context_len,
+ *                    or 0 for a padding row (its rows of out are untouched).
  *   scale            softmax scale (host), finite and > 0.
  *   out              [num_tokens, num_q_heads, head_dim] contiguous.
  * bf16 with head_dim 128 runs on the tcgen05 tensor cores; other cases on a
@@ -306,7 +322,7 @@ PA_API size_t pa_prefill_workspace_size(const pa_cache_desc* desc, int32_t batch
  * pa_validate_metadata -- opt-in device check of the metadata the other calls
  * trust.  Counts, into *error_count (device int32, overwritten), the requests
  * with context_lens outside [1, min(max_context_len, max_pages_per_seq *
- * page_size)], new-token counts that are negative or exceed the context (when
+ * page_size)] (padding rows, context_lens == 0, are not counted), new-token counts that are negative or exceed the context (when
  * cu_seqlens_q is given; may be NULL), and block-table entries outside
  * [0, num_pages) among the pages a request uses.  Never faults; read the count
  * after synchronising.

@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
       if (L >= 1 && L <= cap) {
         cnt = (L + T - 1) >> p.log2T;
       } else {
-        raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
+        // length 0 is a padding row: nothing is read, stored or written for it
+        if (L != 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
         if (p.k_new != nullptr && p.slot_out) p.slot_out[b] = -1;
       }
     }

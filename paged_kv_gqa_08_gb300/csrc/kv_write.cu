@@ -18,6 +18,15 @@ __global__ void __launch_bounds__(128) slot_mapping_kernel(const SlotMapParams p
   const int L = p.context_lens[b];
   const int n = s1 - s0;
   const int start = L - n;
+  if (L == 0 && n >= 0 && s0 >= 0 && static_cast<int64_t>(s1) <= p.num_tokens) {
+    // A padding row (length 0: a batch padded up to a fixed size): its tokens
+    // are stored nowhere.
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      p.positions[s0 + j] = 0;
+      p.slots[s0 + j] = -1;
+    }
+    return;
+  }
   const bool ok = n >= 0 && start >= 0 && s0 >= 0 && static_cast<int64_t>(s1) <= p.num_tokens &&
                   static_cast<int64_t>(L) <= static_cast<int64_t>(p.max_pages) * p.page_size;
   if (!ok) {

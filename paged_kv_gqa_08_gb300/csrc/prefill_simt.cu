@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(128) prefill_simt_kernel(const SimtParams p) {
   if (t < s0 || t >= s1) return;  // malformed cu_seqlens: nothing to do
   const int L = p.ctx[b];
   const int n = s1 - s0;
+  if (L == 0) return;  // a padding row
   if (n > L || L > p.max_ctx || static_cast<int64_t>(L) > static_cast<int64_t>(p.maxp) * p.P) {
     if (lane == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
     return;

@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (2 * qp * p.TQ >= n) return;
   const int L = p.ctx[b];
   const int cap = static_cast<int>(min(static_cast<int64_t>(p.max_ctx), static_cast<int64_t>(p.maxp) << p.log2P));
+  if (L == 0 && s0 >= 0 && s1 <= p.num_tokens) return;  // a padding row
   if (s0 < 0 || s1 > p.num_tokens || L < n || L > cap) {
     if (threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
     return;
@@ -729,7 +730,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
       const int s0 = q.cu[b], s1 = q.cu[b + 1];
       n = s1 - s0;
       L = q.ctx[b];
-      if (s0 < 0 || n < 0 || s1 > q.num_tokens || n > q.max_seqlen_q || L < n || L > q.cap_ctx)
+      const bool padding = L == 0 && s0 >= 0 && n >= 0 && s1 <= q.num_tokens;
+      if (padding)
+        np = 0;
+      else if (s0 < 0 || n < 0 || s1 > q.num_tokens || n > q.max_seqlen_q || L < n || L > q.cap_ctx)
         raise_flag(q.err, PA_DEVERR_BAD_LENGTH);
       else
         np = ((n + q.TQ - 1) / q.TQ + 1) / 2;

@@ -10,6 +10,7 @@ __global__ void __launch_bounds__(128) validate_kernel(const ValidateArgs a) {
   if (b >= a.batch) return;
   int bad = 0;
   const int L = a.context_lens[b];
+  if (L == 0) return;  // a padding row
   const int64_t by_pages = static_cast<int64_t>(a.max_pages) * a.page_size;
   const int64_t cap = a.max_context_len < by_pages ? a.max_context_len : by_pages;
   const bool len_ok = L >= 1 && L <= cap;

@@ -100,20 +100,30 @@ def test_decode_flags_bad_metadata_and_keeps_other_requests_right():
     run.step()
     torch.cuda.synchronize()
     pa_read_device_errors(reset=True)
-    # request 2: an out-of-range page id; request 4: a zero context length
+    # request 2: an out-of-range page id; request 4: a negative context length;
+    # request 1: a padding row (length 0), skipped without a flag
     bt = run.t["block_tables"].clone()
     bt[2, 0] = 10 ** 6
     ctx = run.t["context_lens"].clone()
-    ctx[4] = 0
+    ctx[4] = -3
+    ctx[1] = 0
     out = torch.full_like(run.bufs.out, 7.0)
     pa_decode(run.desc, run.t["q"], wl.batch, run.k_cache, run.v_cache, bt, wl.max_pages_per_seq, ctx,
               wl.max_context_len, wl.scale, 0, out, run.bufs.workspace)
     torch.cuda.synchronize()
     flags = pa_read_device_errors(reset=True)
     assert flags & PA_DEVERR_BAD_PAGE and flags & PA_DEVERR_BAD_LENGTH
-    good = [0, 1, 3, 5]
+    good = [0, 3, 5]
     _check(out[good], ref["o"][good], wl.dtype)
     assert torch.all(out[4] == 7.0)          # skipped request: output untouched
+    assert torch.all(out[1] == 7.0)          # padding row: output untouched
+    # a padding row alone raises nothing
+    bt = run.t["block_tables"].clone()
+    bt[1] = -7
+    pa_decode(run.desc, run.t["q"], wl.batch, run.k_cache, run.v_cache, bt, wl.max_pages_per_seq, ctx.clamp(min=0),
+              wl.max_context_len, wl.scale, 0, out, run.bufs.workspace)
+    torch.cuda.synchronize()
+    assert pa_read_device_errors(reset=True) == 0
 
 
 def test_decode_zero_batch_is_a_no_op():

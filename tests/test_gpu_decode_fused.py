@@ -74,13 +74,14 @@ def test_fused_decode_reports_skipped_requests():
     run = GpuCase(wl)
     pa_read_device_errors(reset=True)
     ctx = run.t["context_lens"].clone()
-    ctx[3] = 0
+    ctx[3] = -2         # bad metadata: skipped and flagged
+    ctx[1] = 0          # a padding row: skipped, slot -1, no flag of its own
     out, slots = _fused(run, wl, ctx=ctx)
-    assert pa_read_device_errors(reset=True) & PA_DEVERR_BAD_LENGTH
+    assert pa_read_device_errors(reset=True) == PA_DEVERR_BAD_LENGTH
     s = slots.cpu().numpy()
     ref = oracle.reference_step(wl)
-    assert s[3] == -1
-    good = [0, 1, 2, 4, 5]
+    assert s[3] == -1 and s[1] == -1
+    good = [0, 2, 4, 5]
     assert np.array_equal(s[good], ref["slots"][good])
     ok, err, bound = oracle.within_tolerance(as_f64(out[good]), ref["o"][good], wl.dtype)
     assert ok, (err, bound)

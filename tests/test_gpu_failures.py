@@ -44,7 +44,9 @@ def test_validate_metadata_counts_problems():
     bt[3, 0] = -5
     bt[6, 1] = wl.num_pages
     ctx = run.t["context_lens"].clone()
-    ctx[2] = 0
+    ctx[2] = -1
+    ctx[5] = 0          # a padding row: not a problem
+    bt[5] = -9          # (its block-table row is never looked at)
     cu = run.t["cu_seqlens_q"].clone()
     pa_validate_metadata(*args, cu, ctx, bt, wl.max_pages_per_seq, wl.max_context_len, cnt)
     torch.cuda.synchronize()

@@ -203,3 +203,69 @@ def test_random_planned_batches_match_oracle(seed):
     ref = oracle.reference_step(wl)
     _check(out[: wl.num_new_tokens], ref["o"], wl.dtype)
     assert pa_read_device_errors(reset=True) == 0
+
+
+@pytest.mark.parametrize("planned", [True, False], ids=["planned", "unplanned"])
+def test_prefill_padding_rows_are_skipped(planned):
+    # Requests 1 and 3 become padding rows (context length 0, block-table rows
+    # that hold no page id): their output rows stay untouched, no flag is
+    # raised, and the other requests are unaffected.
+    spec = dict(kind="prefill", dtype="bf16", B=4, Hq=16, Hkv=8, hd=128, P=16, chunks=[20, 5, 30, 7],
+                prefixes=[100, 40, 0, 300], norm=False, seed=31)
+    wl = synth.make_workload(spec)
+    run = GpuCase(wl, plan_prefill=planned)
+    run.step()
+    torch.cuda.synchronize()
+    pa_read_device_errors(reset=True)
+    ctx = run.t["context_lens"].clone()
+    bt = run.t["block_tables"].clone()
+    for b in (1, 3):
+        ctx[b] = 0
+        bt[b] = -7
+    out = torch.full_like(run.bufs.out, 3.0)
+    pa_prefill_varlen(run.desc, run.t["q"], run.t["cu_seqlens_q"], wl.batch, wl.max_new_len, wl.num_new_tokens,
+                      run.k_cache, run.v_cache, bt, wl.max_pages_per_seq, ctx, wl.max_context_len, wl.scale, out,
+                      run.bufs.workspace)
+    torch.cuda.synchronize()
+    assert pa_read_device_errors(reset=True) == 0
+    cu = wl.cu_seqlens_q
+    rows = {b: list(range(cu[b], cu[b + 1])) for b in range(wl.batch)}
+    ref = oracle.reference_step(wl, requests=[0, 2])
+    _check(out[rows[0] + rows[2]], ref["o"], wl.dtype)
+    assert torch.all(out[rows[1] + rows[3]] == 3.0)
+
+
+PERMUTED = {
+    "mixed_chunks": "qwen3_0p6b_chunked_prefill",
+    "split_key_ranges": dict(kind="prefill", dtype="bf16", B=3, Hq=32, Hkv=4, hd=128, P=32, chunks=[1, 90, 1],
+                             prefixes=[9000, 15000, 31], norm=True, seed=77),
+}
+
+
+@pytest.mark.parametrize("planned", [True, False], ids=["planned", "unplanned"])
+@pytest.mark.parametrize("case", sorted(PERMUTED))
+def test_prefill_page_permutation_is_bitwise_invariant(case, planned):
+    # Moving every page to another physical id (and rewriting the block
+    # tables to match) changes no output bit: the work split and the order
+    # of the arithmetic depend on logical positions only.
+    wl = synth.make_workload(PERMUTED[case])
+    run = GpuCase(wl, plan_prefill=planned)
+    out1 = run.step().clone()
+    if planned:
+        assert _plan_header(run)[1] > 0 or case == "mixed_chunks"
+    g = torch.Generator(device="cuda").manual_seed(5)
+    perm = torch.randperm(wl.num_pages, device="cuda", generator=g)
+    kc2 = torch.empty_like(run.k_cache)
+    vc2 = torch.empty_like(run.v_cache)
+    kc2[perm] = run.k_cache
+    vc2[perm] = run.v_cache
+    bt2 = perm[run.t["block_tables"].long()].to(torch.int32)
+    q = run.bufs.q_out if wl.q_norm_w is not None else run.t["q"]
+    out2 = torch.full_like(out1, float("nan"))
+    pa_prefill_varlen(run.desc, q, run.t["cu_seqlens_q"], wl.batch, wl.max_new_len, wl.num_new_tokens, kc2, vc2, bt2,
+                      wl.max_pages_per_seq, run.t["context_lens"], wl.max_context_len, wl.scale, out2,
+                      run.bufs.workspace)
+    torch.cuda.synchronize()
+    n = wl.num_new_tokens
+    assert torch.equal(out1[:n].view(torch.int16), out2[:n].view(torch.int16))
+    assert pa_read_device_errors(reset=True) == 0
