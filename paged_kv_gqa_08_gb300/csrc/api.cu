@@ -22,11 +22,6 @@ DeviceInfo g_info[kMaxDevices];
 unsigned int* g_err_word[kMaxDevices];
 thread_local int g_last_cuda_error = 0;
 
-pa_status cuda_fail(cudaError_t e) {
-  g_last_cuda_error = static_cast<int>(e);
-  return PA_ERR_CUDA;
-}
-
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -62,6 +57,28 @@ pa_status prepare(unsigned int** err) {
 }
 
 }  // namespace
+
+pa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
+}
+
+pa_status check_decode_args(const pa_cache_desc* d, const void* q, int32_t batch, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables, int32_t max_pages_per_seq,
+                            const int32_t* context_lens, int32_t max_context_len, float scale, int32_t max_ctas,
+                            const void* out) {
+  pa_status st = check_desc(d);
+  if (st != PA_OK) return st;
+  if (batch < 0 || max_ctas < 0) return PA_ERR_SHAPE;
+  if (batch == 0) return PA_OK;
+  if (max_pages_per_seq < 1 || max_context_len < 1) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * d->page_size)
+    return PA_ERR_SHAPE;
+  if (!isfinite(scale)) return PA_ERR_SHAPE;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
 
 cudaError_t current_device_info(DeviceInfo* out) {
   int dev = 0;
@@ -240,16 +257,9 @@ pa_status pa_decode(const pa_cache_desc* desc, const void* q, int32_t batch, con
                     const void* v_cache, const int32_t* block_tables, int32_t max_pages_per_seq,
                     const int32_t* context_lens, int32_t max_context_len, float scale, int32_t max_ctas, void* out,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (batch < 0 || max_ctas < 0) return PA_ERR_SHAPE;
-  if (batch == 0) return PA_OK;
-  if (max_pages_per_seq < 1 || max_context_len < 1) return PA_ERR_SHAPE;
-  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * desc->page_size)
-    return PA_ERR_SHAPE;
-  if (!isfinite(scale)) return PA_ERR_SHAPE;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
+  pa_status st = check_decode_args(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens,
+                                   max_context_len, scale, max_ctas, out);
+  if (st != PA_OK || batch == 0) return st;
   if (!workspace) return PA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGN;
   unsigned int* err = nullptr;

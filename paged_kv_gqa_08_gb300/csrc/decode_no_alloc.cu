@@ -10,8 +10,13 @@
 // caches, the metadata and the output.
 //
 // The scratch is a file-scope __device__ array of kNoAllocScratchBytes
-// (16 MiB); every device that loads the library holds it until the process
-// exits.  Every call shares it and it keeps the last call's contents; nothing
+// (16 MiB); every device that loads the library's code holds it until the
+// process exits.  Under lazy module loading (CUDA_MODULE_LOADING=LAZY, the
+// runtime's default) the array is placed in device memory only when its
+// address is first looked up, which the first call of this entry point on
+// each device does: make that call early, before the caller's memory manager
+// takes the rest of the device heap and before any stream capture.  Later
+// calls look up nothing and touch no allocator.  Every call shares it and it keeps the last call's contents; nothing
 // in it needs to start at zero (each call's plan kernel rewrites the metadata
 // the decode and merge kernels read, and every partial is written before it is
 // read), but calls that overlap on the GPU -- on two streams, or from two
@@ -55,34 +60,6 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
-bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// The same host-side checks as pa_decode, minus the workspace arguments.
-pa_status check_args(const pa_cache_desc* d, const void* q, int32_t batch, const void* k_cache, const void* v_cache,
-                     const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
-                     int32_t max_context_len, float scale, int32_t max_ctas, const void* out) {
-  if (!d) return PA_ERR_NULL;
-  if (d->dtype != PA_F32 && d->dtype != PA_BF16) return PA_ERR_DTYPE;
-  if (d->num_q_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 || d->page_size < 1 || d->num_pages < 1)
-    return PA_ERR_SHAPE;
-  if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_SHAPE;
-  if (d->head_dim != 64 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (!pow2(d->num_kv_heads) || d->num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
-  if (d->num_q_heads / d->num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
-  if (!pow2(d->page_size) || d->page_size < 16) return PA_ERR_UNSUPPORTED;
-  if (d->num_pages > (int64_t(1) << 40) / d->page_size) return PA_ERR_SHAPE;
-  if (batch < 0 || max_ctas < 0) return PA_ERR_SHAPE;
-  if (batch == 0) return PA_OK;
-  if (max_pages_per_seq < 1 || max_context_len < 1) return PA_ERR_SHAPE;
-  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * d->page_size)
-    return PA_ERR_SHAPE;
-  if (!isfinite(scale)) return PA_ERR_SHAPE;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
-  if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(out)) return PA_ERR_ALIGN;
-  return PA_OK;
-}
-
 }  // namespace
 }  // namespace pa
 
@@ -93,21 +70,21 @@ extern "C" pa_status pa_decode_no_alloc(const pa_cache_desc* desc, const void* q
                                         int32_t max_pages_per_seq, const int32_t* context_lens,
                                         int32_t max_context_len, float scale, int32_t max_ctas, void* out,
                                         pa_stream_t stream) {
-  pa_status st = check_args(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens,
-                            max_context_len, scale, max_ctas, out);
+  pa_status st = check_decode_args(desc, q, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens,
+                                   max_context_len, scale, max_ctas, out);
   if (st != PA_OK || batch == 0) return st;
   (void)cudaGetLastError();
   unsigned int* err = nullptr;
   cudaError_t e = device_error_word(&err);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   DecodePlan pl;
   e = plan_decode(*desc, batch, max_context_len, max_ctas, &pl);
   if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   if (pl.ws_bytes > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;  // batch too large for the fixed scratch
   void* scratch = nullptr;
   e = scratch_address(&scratch);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e);
   DecodeArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -122,5 +99,5 @@ extern "C" pa_status pa_decode_no_alloc(const pa_cache_desc* desc, const void* q
   a.max_context_len = max_context_len;
   a.scale = scale;
   e = launch_decode(*desc, pl, a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }

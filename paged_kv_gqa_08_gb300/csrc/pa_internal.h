@@ -23,6 +23,18 @@ cudaError_t current_device_info(DeviceInfo* out);
 // Address of the device error word on the current device.
 cudaError_t device_error_word(unsigned int** out);
 
+// Records `e` as the calling thread's last CUDA error (pa_last_cuda_error)
+// and returns PA_ERR_CUDA; every entry point's PA_ERR_CUDA goes through it.
+pa_status cuda_fail(cudaError_t e);
+
+// Host-side checks shared by the decode entry points: the descriptor, the
+// sizes, the scale and the pointers pa_decode takes (its workspace aside).
+// PA_OK with batch == 0 means "nothing to do".
+pa_status check_decode_args(const pa_cache_desc* d, const void* q, int32_t batch, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables, int32_t max_pages_per_seq,
+                            const int32_t* context_lens, int32_t max_context_len, float scale, int32_t max_ctas,
+                            const void* out);
+
 inline int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 
 // ---------------------------------------------------------------------------
