@@ -7,39 +7,52 @@
 // chunk sits at position context_lens[b] - n_b + i and attends to keys
 // 0 .. that position, all read from the paged cache.
 //
-// One CTA = (request, kv-head, pair of q-tiles).  A q-tile is 128 rows:
-// TQ = 128 / G tokens x the G q-heads that share the kv-head, so each staged
-// K/V tile feeds the whole GQA group, and it feeds both q-tiles of the pair
-// (256 rows per K/V tile).
-//   warp 0     TMA producer of Q and K: both Q tiles once (3-D map) and K
-//              tile 0 go out during the CTA's setup, then per 128-key tile
-//              the K rows gathered page by page with 16-row boxes
-//              (single-row boxes for a ragged end, so no slot past the context
-//              is read); block-table entries are read one tile ahead.
-//   warp 10    TMA producer of V, the same way; K and V run ahead of the MMAs
-//              independently, each as far as its own two stages allow.
-//   warp 1     allocates all 512 TMEM columns; lane 0 issues the MMAs:
-//              S_g = Q_g K_j^T and O_g += P_g V_j for the two q-tiles g, in
-//              the order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), so that each
-//              softmax group has a PV and a QK of the other group to hide in.
-//   warps 2-9  two softmax groups of 4 warps, one thread per row (= TMEM
+// Work item = (q-tile pair of a request, kv-head, range of 128-key tiles).  A
+// q-tile is 128 rows: TQ = 128 / G tokens x the G q-heads that share the
+// kv-head, so each staged K/V tile feeds the whole GQA group.  A pair with
+// two q-tiles runs in pair mode: each K/V tile feeds both (256 rows).  A
+// pair with one q-tile (a short chunk) runs in split mode: its key tiles
+// alternate between the two softmax groups, each keeping its own O and row
+// statistics, and the first group merges the two halves at the end.
+//
+// Planned launch (the caller gives a workspace): a one-CTA planner kernel
+// lists the pairs, cuts long key ranges into parts and lists the units
+// longest first; the attention kernel is persistent -- one CTA per SM takes
+// items (unit x kv-head) from a shared counter as it frees up -- and a part
+// writes O / l and the row log-sum-exp in fp32 for a merge kernel that
+// combines the parts of each split pair (flash-decoding's split-KV rule,
+// applied to prefill rows).  Without a workspace, each CTA runs its own
+// pair's item with all its keys.
+//
+// Warp roles (12 warps):
+//   warps 0-7  two softmax groups of 4 warps, one thread per row (= TMEM
 //              lane): a tile's 128 scores come into registers in one TMEM
 //              round trip, the row max is taken, O in TMEM is rescaled only
 //              when a row max grows by more than 2^8, and the bf16
 //              probabilities are written back over S's first 64 columns,
-//              where the PV MMA reads its A operand.  Finally O / l goes to
-//              global memory.
+//              where the PV MMA reads its A operand.  At an item's end O / l
+//              goes to global memory (O is released to the next item as soon
+//              as it is in registers).
+//   warp 8     TMA producer of Q and K: an item's Q tiles (3-D map), then
+//              per 128-key tile the K rows gathered page by page with 16-row
+//              boxes (single-row boxes for a ragged end, so no slot past the
+//              context is read); block-table entries are read one tile ahead.
+//   warp 9     TMA producer of V, the same way; K and V run ahead of the MMAs
+//              independently in two-stage rings that continue across items.
+//   warp 10    allocates all 512 TMEM columns; lane 0 issues the MMAs:
+//              S_g = Q K^T and O_g += P_g V for the two groups, in the order
+//              PV_0, QK_0 of the next step, PV_1, QK_1 of the next step, so
+//              that each softmax group has a PV and a QK of the other group
+//              to hide in.
+//   warp 11    work scheduler: takes the next item when the CTA's current
+//              item has all its K tiles issued, and hands it to the others
+//              through a two-slot ring in shared memory.
+// The softmax warpgroups run with 200 registers, the warpgroup of warps 8-11
+// with 104 (setmaxnreg; the launch gives 168 to every thread).
 // TMEM: S_0 cols 0-127 (P_0 in 0-63), S_1 128-255 (P_1 in 128-191),
 //       O_0 256-383, O_1 384-511.
 // Every wait is bounded; a timeout raises PA_DEVERR_TIMEOUT and the CTA
 // drains its copies and MMAs, frees its TMEM and returns.
-//
-// Planned launch (the caller gives a workspace): a one-CTA planner kernel
-// turns the pairs into units, cutting long key ranges into parts and listing
-// the units longest first; a CTA then runs one (unit, kv-head), a part writes
-// O / l and the row log-sum-exp in fp32, and a merge kernel combines the
-// parts of each split pair (flash-decoding's split-KV rule, applied to
-// prefill rows).
 #include <cuda.h>
 #include <limits.h>
 #include <math.h>
@@ -47,6 +60,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "pa_common.cuh"
 
@@ -57,16 +71,31 @@ constexpr int kBM = 128;                    // rows per q-tile
 constexpr int kBN = 128;                    // keys per tile
 constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 bf16 (one swizzle-atom column)
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
-constexpr int kThreads = 352;  // warp 0 K copies, 1 MMA, 2-9 softmax, 10 V copies
-constexpr int kVWarp = 10;
+// warps 0-3 softmax group 0, 4-7 softmax group 1, 8 Q and K copies, 9 V copies,
+// 10 MMA issuer, 11 work scheduler
+constexpr int kThreads = 384;
+constexpr int kKWarp = 8, kVWarp = 9, kMmaWarp = 10, kSchedWarp = 11;
+constexpr int kItemConsumers = 11;  // warps that take each work item: the copies, the MMA issuer, 8 softmax
+// Per-thread registers: at launch (the kernel must be built with exactly this
+// many; the host checks), and after the warpgroups rebalance.
+constexpr int kLaunchRegs = 168, kSoftmaxRegs = 200, kRoleRegs = 104;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kRoleRegs <= kThreads * kLaunchRegs,
+              "the rebalanced registers fit in the launch allocation");
 constexpr int kBoxRows = 16;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr int kOffQ = 0;                          // two q-tiles
 constexpr int kOffK = kOffQ + 2 * kTileBytes;     // two K stages
 constexpr int kOffV = kOffK + 2 * kTileBytes;     // two V stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + slack to align the base to 1024
+constexpr int kOffBar = kOffV + 2 * kTileBytes;   // 26 mbarriers
+// indices of the mbarriers in their table (pairs are [2], one per stage or group)
+constexpr int kBarItemFull = 0, kBarItemEmpty = 2, kBarQFull = 4, kBarQEmpty = 5, kBarKFull = 6, kBarKEmpty = 8,
+              kBarVFull = 10, kBarVEmpty = 12, kBarSFull = 14, kBarPFull = 16, kBarPvDone = 18, kBarOFree = 20,
+              kBarMlFull = 22, kBarMlEmpty = 23, kBarMmaDone = 24, kBarSchedGo = 25;
+constexpr int kOffItem = kOffBar + 256;           // two work items
+constexpr int kOffMl = kOffItem + 256;            // 128 (max, sum) rows handed between the softmax groups
+constexpr int kOffMisc = kOffMl + 128 * 8;        // TMEM base address, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, M = 128, N = 128.
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
@@ -87,13 +116,14 @@ struct TcParams {
   int64_t num_pages, num_tokens;
   int32_t B, Hq, Hkv, G, TQ, P, log2P, maxp, max_ctx;
   float scale_log2;
-  // Planned launch (all null without a workspace): CTA x of the 1-D grid runs
-  // kv-head x % Hkv of unit x / Hkv, units[u] = {request, q-tile pair,
+  // Planned launch (all null without a workspace): the CTAs take work items
+  // k = unit * Hkv + kv-head from *counter, units[u] = {request, q-tile pair,
   // first key tile | (end key tile << 16), partial slot or -1}.  A unit with a
   // slot covers part of its pair's keys and writes O / l and the base-2
   // log-sum-exp of each row to o_part / lse_part for the merge kernel.
   const int4* units;
   const int32_t* n_units;
+  int32_t* counter;  // next item to hand out (zeroed by the planner)
   float* o_part;    // [slot][Hkv][2 q-tiles][128 rows][128]
   float* lse_part;  // [slot][Hkv][2 q-tiles][128 rows]
 };
@@ -120,20 +150,6 @@ PA_DEVINL void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z
 PA_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 PA_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 PA_DEVINL void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 descriptor version 1).
-PA_DEVINL uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-PA_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc)
-      : "memory");
-}
 
 PA_DEVINL void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -181,15 +197,6 @@ PA_DEVINL void drain(uint64_t* bar, uint32_t parity) {
 }
 
 
-// O += A(TMEM) * B(smem): the A operand (probabilities) is read from tensor memory.
-PA_DEVINL void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 // Load 32 columns without waiting; the registers are valid only after
 // tmem_wait_ld32 on the same array, whose asm reads and rewrites them so the
 // compiler cannot move any use above the wait.
@@ -232,285 +239,305 @@ PA_DEVINL float ex2(float x) {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+// One (unit, kv-head) of work, as the scheduler warp hands it to the others.
+struct Item {
+  int32_t valid;    // 0: no more work for this CTA
+  int32_t b, h, qp; // request, kv-head, q-tile pair
+  int32_t j_lo, nt; // key tiles [j_lo, j_lo + nt)
+  int32_t slot;     // partial-result slot of a split pair, or -1
+  int32_t s0;       // the request's first packed row
+  int32_t nq;       // q-tiles of the pair with rows (1 or 2)
+  int32_t split;    // 1: one q-tile whose key tiles alternate between the two softmax groups
+  int32_t c[2];     // key tiles softmax group g processes
+  int32_t qt[2];    // q-tile of the pair (0 or 1) group g works on
+  int32_t rows[2];  // live tokens of that q-tile
+  int32_t pos0[2];  // position of its first token
+  int32_t kv_len;   // keys the pair needs (last token's position + 1)
+  int32_t pad[5];
+};
+static_assert(sizeof(Item) == 96, "two items fit their shared-memory slot");
 
-  int h, b, qp, j_lo = 0, j_hi = 1 << 30, slot = -1;
-  if (p.units) {
-    pdl_wait();     // the planner's unit list is complete
-    pdl_trigger();  // the merge kernel may start launching; it waits for this grid
-    const int u = static_cast<int>(blockIdx.x) / p.Hkv;
-    h = static_cast<int>(blockIdx.x) - u * p.Hkv;
-    if (u >= *p.n_units) return;
-    const int4 ud = p.units[u];
-    b = ud.x;
-    qp = ud.y;
-    j_lo = ud.z & 0xffff;
-    j_hi = static_cast<int>(static_cast<uint32_t>(ud.z) >> 16);
-    slot = ud.w;
-  } else {
-    h = blockIdx.y;
-    b = blockIdx.z;
-    qp = blockIdx.x;
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// The work of pair qp of request b for kv-head h over key tiles [j_lo, j_hi).
+// False when there is none (a padding row, an empty range, a pair without
+// rows) or the request's lengths are inconsistent (flagged).
+PA_DEVINL bool make_item(const TcParams& p, int b, int qp, int h, int j_lo, int j_hi, int slot, Item& it) {
   const int s0 = p.cu[b], s1 = p.cu[b + 1];
   const int n = s1 - s0;
-  if (2 * qp * p.TQ >= n) return;
   const int L = p.ctx[b];
+  if (L == 0 && s0 >= 0 && s1 <= p.num_tokens) return false;  // a padding row
   const int cap = static_cast<int>(min(static_cast<int64_t>(p.max_ctx), static_cast<int64_t>(p.maxp) << p.log2P));
-  if (L == 0 && s0 >= 0 && s1 <= p.num_tokens) return;  // a padding row
-  if (s0 < 0 || s1 > p.num_tokens || L < n || L > cap) {
-    if (threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
-    return;
+  if (s0 < 0 || s1 > p.num_tokens || n < 0 || L < n || L > cap) {
+    raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
+    return false;
   }
-  const int nq = (2 * qp + 1) * p.TQ < n ? 2 : 1;  // q-tiles of the pair with rows
+  if (2 * qp * p.TQ >= n) return false;
+  const int nq = (2 * qp + 1) * p.TQ < n ? 2 : 1;
   int rows[2], pos0[2], ntg[2];
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     const int qt = 2 * qp + g;
-    rows[g] = g < nq ? min(p.TQ, n - qt * p.TQ) : 0;   // live tokens of the tile
-    pos0[g] = L - n + qt * p.TQ;                       // position of its first token
-    ntg[g] = g < nq ? (pos0[g] + rows[g] + kBN - 1) / kBN : 0;  // key tiles it needs
+    rows[g] = g < nq ? min(p.TQ, n - qt * p.TQ) : 0;
+    pos0[g] = L - n + qt * p.TQ;
+    ntg[g] = g < nq ? (pos0[g] + rows[g] + kBN - 1) / kBN : 0;
   }
-  // This unit's key tiles: [j_lo, j_hi) of the pair's [0, ntg).  ntl[g] is the
-  // number q-tile g processes; local tile index jl = j - j_lo.
-  const int kv_len = pos0[nq - 1] + rows[nq - 1];
   j_hi = min(j_hi, ntg[nq - 1]);
   const int nt = j_hi - j_lo;
-  if (nt <= 0) return;
-  int ntl[2];
+  if (nt <= 0) return false;
+  it.valid = 1;
+  it.b = b;
+  it.h = h;
+  it.qp = qp;
+  it.j_lo = j_lo;
+  it.nt = nt;
+  it.slot = slot;
+  it.s0 = s0;
+  it.nq = nq;
+  it.split = nq == 1;
+  it.kv_len = pos0[nq - 1] + rows[nq - 1];
+  if (it.split) {
+    it.c[0] = (nt + 1) / 2;
+    it.c[1] = nt / 2;
 #pragma unroll
-  for (int g = 0; g < 2; ++g) ntl[g] = max(0, min(j_hi, ntg[g]) - j_lo);
-
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = bars + 3;
-  uint64_t* k_empty = bars + 5;
-  uint64_t* v_empty = bars + 7;
-  uint64_t* s_full = bars + 9;    // per q-tile
-  uint64_t* p_full = bars + 11;   // per q-tile
-  uint64_t* pv_done = bars + 13;  // per q-tile
-  uint64_t* o_final = bars + 15;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16) + 1;
-
-  // Producer lane geometry.  Block-table entries are read one tile ahead: the
-  // loads for tile j + 1 are issued before tile j's stage waits, so their
-  // latency is hidden behind them; tile 0's are read before the setup below.
-  // kNoPage marks an entry the lane does not need.
-  const bool producer = warp == 0 || warp == kVWarp;
-  const bool vrole = warp == kVWarp;
-  const int64_t bt_row = static_cast<int64_t>(b) * p.maxp;
-  const int box = lane >> 2, half = (lane >> 1) & 1, isv = lane & 1;
-  const int x = h * 128 + half * 64;
-  constexpr int kNoPage = INT_MIN;
-  auto load_pages = [&](int jj, int& pg_full, int& pg_rem) {
-    const int t0 = (j_lo + jj) * kBN;
-    const int valid = min(kBN, kv_len - t0);
-    const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
-    pg_full = box < nfull ? p.bt[bt_row + ((t0 + box * kBoxRows) >> p.log2P)] : kNoPage;
-    pg_rem = rem && lane < 4 ? p.bt[bt_row + ((t0 + nfull * kBoxRows) >> p.log2P)] : kNoPage;
-  };
-  int pf_next = kNoPage, pr_next = kNoPage;
-  if (producer) load_pages(0, pf_next, pr_next);
-
-  // V rows past the last key are never loaded but meet a probability of 0 in
-  // the PV products, so they must hold finite values: zero both V stages.  Q
-  // needs nothing (and is loaded during this setup): a q-tile in use is always
-  // a whole TMA box, and an unused one is never read.
-  {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads)
-      reinterpret_cast<uint4*>(smem + kOffV)[i] = z;
-  }
-  fence_async_smem();
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 4);
-      mbar_init(&pv_done[s], 1);
-    }
-    mbar_init(o_final, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-    // both Q tiles, issued before the setup barrier so that their latency overlaps it
-    mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nq * 2 * p.G * p.TQ * 128));
-    for (int g = 0; g < nq; ++g) {
-      const int z = s0 + (2 * qp + g) * p.TQ;
-      tma_load_3d(smem + kOffQ + g * kTileBytes, &p.tm_q, 0, h * p.G, z, q_full);
-      tma_load_3d(smem + kOffQ + g * kTileBytes + kHalfBytes, &p.tm_q, 64, h * p.G, z, q_full);
-    }
-  }
-
-  // One K or V tile (by the role of the calling producer warp): page ids ->
-  // rows of the cache, the stage's byte count, then one TMA box per lane.
-  // False when the stage wait ran out.
-  auto issue_tile = [&](int j, int pf, int pr) -> bool {
-    const int st = j & 1;
-    const uint32_t par = ((j >> 1) & 1) ^ 1;
-    const int t0 = (j_lo + j) * kBN;
-    const int valid = min(kBN, kv_len - t0);
-    const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
-    int y_full = -1, y_rem = -1;
-    if (pf != kNoPage) {
-      const int key0 = t0 + box * kBoxRows;
-      if (pf >= 0 && pf < p.num_pages) y_full = (pf << p.log2P) + (key0 & (p.P - 1));
-      else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
-    }
-    if (pr != kNoPage) {
-      const int key0 = t0 + nfull * kBoxRows;
-      if (pr >= 0 && pr < p.num_pages) y_rem = (pr << p.log2P) + (key0 & (p.P - 1));
-      else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
-    }
-    uint32_t mine = (y_full >= 0 ? kBoxRows * 128 : 0) + (y_rem >= 0 ? rem * 128 : 0);
-    uint32_t bytes = (isv != 0) == vrole ? mine : 0;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-    uint64_t* full = vrole ? &v_full[st] : &k_full[st];
-    int okw = 1;
-    if (lane == 0) {
-      okw = mbar_wait_bounded(vrole ? &v_empty[st] : &k_empty[st], par, abort_flag, p.err);
-      if (okw) mbar_arrive_expect_tx(full, bytes);
-    }
-    if (__shfl_sync(0xffffffffu, okw, 0) == 0) return false;
-    if ((isv != 0) == vrole) {
-      unsigned char* dst = smem + (vrole ? kOffV : kOffK) + st * kTileBytes + half * kHalfBytes;
-      const CUtensorMap* m16 = vrole ? &p.tm_v16 : &p.tm_k16;
-      const CUtensorMap* m1 = vrole ? &p.tm_v1 : &p.tm_k1;
-      if (y_full >= 0) tma_load_2d(dst + box * kBoxRows * 128, m16, x, y_full, full);
-      if (y_rem >= 0)
-        for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, m1, x, y_rem + r, full);
-    }
-    return true;
-  };
-  // K tile 0 goes out before the setup barrier as well (the K region is not
-  // zeroed, and a stage's first wait passes at once)
-  int k_first = 0;
-  if (warp == 0) {
-    __syncwarp();  // lane 0's barrier initialisation is visible to the warp
-    const int pf = pf_next, pr = pr_next;
-    if (nt > 1) load_pages(1, pf_next, pr_next);
-    if (issue_tile(0, pf, pr)) k_first = 1;
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  cta_sync();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-
-  if (warp == 0 || warp == kVWarp) {
-    // ------------------------------- TMA producers -------------------------------
-    // warp 0 copies Q and the K tiles, warp kVWarp the V tiles; each runs ahead
-    // as far as its own stages allow
-    int issued = vrole ? 0 : k_first;
-    bool ok = vrole || k_first == 1;
-    for (int j = issued; j < nt && ok; ++j) {
-      const int pf = pf_next, pr = pr_next;
-      if (j + 1 < nt) load_pages(j + 1, pf_next, pr_next);
-      ok = issue_tile(j, pf, pr);
-      if (ok) ++issued;
-    }
-    if (!ok && lane == 0) {
-      if (!vrole) drain(q_full, 0);
-      uint64_t* full = vrole ? v_full : k_full;
-      for (int j = max(0, issued - 2); j < issued; ++j) drain(&full[j & 1], (j >> 1) & 1);
-    }
-  } else if (warp == 1) {
-    // ------------------------------- MMA issuer -------------------------------
-    if (lane == 0) {
-      bool ok = mbar_wait_bounded(q_full, 0, abort_flag, p.err);
-      const uint32_t aQ = smem_u32(smem + kOffQ);
-      const uint32_t aK = smem_u32(smem + kOffK), aV = smem_u32(smem + kOffV);
-      auto qk = [&](int g, int j) {
-        const uint32_t qbase = aQ + g * kTileBytes, kbase = aK + (j & 1) * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          mma_bf16(tmem + g * 128, sdesc(qbase + off, 16, 1024), sdesc(kbase + off, 16, 1024), kIdescQK, k > 0);
-        }
-        mma_commit(&s_full[g]);
-      };
-      auto pv = [&](int g, int j) -> bool {
-        if (!mbar_wait_bounded(&p_full[g], j & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t vbase = aV + (j & 1) * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16_ts(tmem + 256 + g * 128, tmem + g * 128 + k * 8, sdesc(vbase + k * 16 * 128, kHalfBytes, 1024),
-                      kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&pv_done[g]);
-        return true;
-      };
-      if (ok) ok = mbar_wait_bounded(&k_full[0], 0, abort_flag, p.err);
-      if (ok) {
-        tc_fence_after();
-        for (int g = 0; g < nq; ++g)
-          if (ntl[g] > 0) qk(g, 0);
-        mma_commit(&k_empty[0]);
-      }
-      for (int j = 0; j < nt && ok; ++j) {
-        const bool more = j + 1 < nt;
-        if (!(ok = mbar_wait_bounded(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.err))) break;
-        // q-tile 0: PV of tile j, then QK of tile j+1 (the tensor pipe runs them
-        // in issue order, so QK overwrites S_0 only after PV has read P_0)
-        if (j < ntl[0] && !(ok = pv(0, j))) break;
-        if (more) {
-          if (!(ok = mbar_wait_bounded(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.err))) break;
-          tc_fence_after();
-          if (j + 1 < ntl[0]) qk(0, j + 1);
-        }
-        // q-tile 1
-        if (j < ntl[1] && !(ok = pv(1, j))) break;
-        if (more && j + 1 < ntl[1]) qk(1, j + 1);
-        mma_commit(&v_empty[j & 1]);
-        if (more) mma_commit(&k_empty[(j + 1) & 1]);
-      }
-      mma_commit(o_final);
-      if (!ok) drain(o_final, 0);
+    for (int g = 0; g < 2; ++g) {
+      it.qt[g] = 0;
+      it.rows[g] = rows[0];
+      it.pos0[g] = pos0[0];
     }
   } else {
-    // ------------------------------- softmax groups -------------------------------
-    const int g = (warp - 2) >> 2;
-    const int wq = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t colS = g * 128, colO = 256 + g * 128;
-    const int t = row / p.G, gg = row - (row / p.G) * p.G;
-    const bool live = g < nq && row < p.TQ * p.G && t < rows[g];
-    const int pos_r = pos0[g] + t;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      it.c[g] = max(0, min(j_hi, ntg[g]) - j_lo);
+      it.qt[g] = g;
+      it.rows[g] = rows[g];
+      it.pos0[g] = pos0[g];
+    }
+  }
+  return true;
+}
+
+// Wait (lane 0) for work item i, copy it to every lane and release its slot.
+// False when the wait ran out.
+PA_DEVINL bool take_item(Item* items, uint64_t* item_full, uint64_t* item_empty, int i, volatile int* abort_flag,
+                         unsigned int* err, Item& it) {
+  const int s = i & 1;
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(&item_full[s], (i >> 1) & 1, abort_flag, err);
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+  it = items[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&item_empty[s]);
+  return true;
+}
+
+// The same for a role that runs on one lane (the MMA issuer).
+PA_DEVINL bool take_item_lane(Item* items, uint64_t* item_full, uint64_t* item_empty, int i,
+                              volatile int* abort_flag, unsigned int* err, Item& it) {
+  const int s = i & 1;
+  if (!mbar_wait_bounded(&item_full[s], (i >> 1) & 1, abort_flag, err)) return false;
+  it = items[s];
+  mbar_arrive(&item_empty[s]);
+  return true;
+}
+
+
+
+// mbarrier helpers on 32-bit shared-memory addresses (the MMA issuer names its
+// barriers as base + 8 * index, so no 64-bit pointers stay live).
+PA_DEVINL bool try_wait_a(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+PA_DEVINL bool wait_a(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* err) {
+  if (try_wait_a(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (try_wait_a(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        raise_flag(err, PA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+PA_DEVINL void commit_a(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// The 8 MMAs (k = 16 dims each) of S = Q K^T for one 128 x 128 tile, and of
+// O (+)= P V with P from tensor memory.  An operand descriptor is passed as
+// its low 32 bits (address >> 4 and leading offset), the high half being the
+// same for every operand here (stride 1024, descriptor version, 128-byte
+// swizzle); the k-th operand is the tile's low half plus its address offset >> 4.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+PA_DEVINL uint32_t desc_lo(uint32_t saddr, uint32_t lbo) { return ((saddr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16); }
+
+PA_DEVINL void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(acc), "n"(kDescHi)
+      : "memory");
+}
+
+PA_DEVINL void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(acc), "n"(kDescHi)
+      : "memory");
+}
+
+PA_DEVINL void issue_qk(uint32_t d_s, uint32_t a_lo, uint32_t b_lo) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t off = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
+    mma_ss(d_s, a_lo + off, b_lo + off, kIdescQK, k > 0);
+  }
+}
+
+PA_DEVINL void issue_pv(uint32_t d_o, uint32_t a_p, uint32_t v_lo, bool first) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    mma_ts(d_o, a_p + k * 8, v_lo + ((k * 16 * 128) >> 4), kIdescPV, (!first || k > 0) ? 1u : 0u);
+}
+
+// 32-byte global stores (one whole sector per lane).
+PA_DEVINL void stg32(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4, uint32_t a5,
+                     uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a0), "r"(a1), "r"(a2),
+               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
+// O columns [32 * Q0, 32 * Q0 + N) of a row to global memory, scaled by a:
+// fp32 into the part's slot row, or bf16 into the output row when the row is
+// live (all indices known at compile time, so `o` stays in registers).
+template <int Q0, int N>
+PA_DEVINL void store_cols(const uint32_t (&o)[N], float a, bool part, bool live, float* part_row, char* out_row,
+                          bool out32) {
+  auto f = [&](int e) { return __uint_as_float(o[e]) * a; };
+  if (part) {
+    float* dstp = part_row + 32 * Q0;
+#pragma unroll
+    for (int q8 = 0; q8 < N / 8; ++q8)
+      stg32(dstp + 8 * q8, __float_as_uint(f(8 * q8)), __float_as_uint(f(8 * q8 + 1)), __float_as_uint(f(8 * q8 + 2)),
+            __float_as_uint(f(8 * q8 + 3)), __float_as_uint(f(8 * q8 + 4)), __float_as_uint(f(8 * q8 + 5)),
+            __float_as_uint(f(8 * q8 + 6)), __float_as_uint(f(8 * q8 + 7)));
+  } else if (live) {
+#pragma unroll
+    for (int q16 = 0; q16 < N / 16; ++q16) {
+      const int e = 16 * q16;
+      const uint32_t w0 = pack_bf16x2(f(e), f(e + 1)), w1 = pack_bf16x2(f(e + 2), f(e + 3));
+      const uint32_t w2 = pack_bf16x2(f(e + 4), f(e + 5)), w3 = pack_bf16x2(f(e + 6), f(e + 7));
+      const uint32_t w4 = pack_bf16x2(f(e + 8), f(e + 9)), w5 = pack_bf16x2(f(e + 10), f(e + 11));
+      const uint32_t w6 = pack_bf16x2(f(e + 12), f(e + 13)), w7 = pack_bf16x2(f(e + 14), f(e + 15));
+      char* dst = out_row + Q0 * 64 + q16 * 32;
+      if (out32) {
+        stg32(dst, w0, w1, w2, w3, w4, w5, w6, w7);
+      } else {  // an output only 16-byte aligned
+        stg16(dst, make_uint4(w0, w1, w2, w3));
+        stg16(dst + 16, make_uint4(w4, w5, w6, w7));
+      }
+    }
+  }
+}
+
+struct SoftmaxArgs {
+  char* out;
+  bool out32;  // out is 32-byte aligned (whole-sector stores)
+  float* o_part;
+  float* lse_part;
+  unsigned int* err;
+  int32_t Hq, Hkv, G, TQ;
+  float scale_log2;
+};
+
+// The two softmax warpgroups (warps 0-7).  A function of its own, entered
+// after the warpgroups' register rebalance, so that it is compiled for the
+// larger register budget.
+__device__ __noinline__ void softmax_role(const SoftmaxArgs p, unsigned char* smem, uint32_t tmem, int warp,
+                                          int lane) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* item_full = bars + kBarItemFull;
+  uint64_t* item_empty = bars + kBarItemEmpty;
+  uint64_t* s_full = bars + kBarSFull;
+  uint64_t* p_full = bars + kBarPFull;
+  uint64_t* pv_done = bars + kBarPvDone;
+  uint64_t* o_free = bars + kBarOFree;
+  uint64_t* ml_full = bars + kBarMlFull;
+  uint64_t* ml_empty = bars + kBarMlEmpty;
+  Item* items = reinterpret_cast<Item*>(smem + kOffItem);
+  float2* ml = reinterpret_cast<float2*>(smem + kOffMl);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc) + 1;
+  // ------------------------------- softmax groups -------------------------------
+  // Group g (warps 4g .. 4g+3) owns S_g / O_g; a thread owns one row (TMEM
+  // lane).  Pair mode: group g works on q-tile g with all its key tiles.
+  // Split mode (one q-tile): both groups work on q-tile 0, group g on the
+  // item's key tiles g, g+2, g+4, ...; group 0's epilogue merges the two
+  // partial results (the split-KV rule within one CTA).
+  const int g = warp >> 2;
+  const int wq = warp & 3;  // TMEM lane quarter this warp may access
+  const int row = wq * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t colS = g * 128, colO = 256 + g * 128;
+  const int t_r = row / p.G, gg = row - (row / p.G) * p.G;
+  int sc = 0;          // S tiles this group has consumed
+  int pc[2] = {0, 0};  // PVs issued per group before the current item
+  int ms = 0;          // split-mode items done
+  bool ok = true;
+  for (int i = 0; ok; ++i) {
+    Item it;
+    if (!take_item(items, item_full, item_empty, i, abort_flag, p.err, it)) {
+      ok = false;
+      break;
+    }
+    if (!it.valid) break;
+    const int c0 = it.c[0], c1 = it.c[1];
+    const int c = g ? c1 : c0;
+    const int p0 = g ? it.pos0[1] : it.pos0[0];
+    const int qtg = g ? it.qt[1] : it.qt[0];
+    const int pos_r = p0 + t_r;
+    const bool live = row < p.TQ * p.G && t_r < (g ? it.rows[1] : it.rows[0]);
+    const int j_lo = it.j_lo, split = it.split, slot = it.slot, hh_kv = it.h;
+    const int it_qp = it.qp, it_s0 = it.s0;
     float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < ntl[g]; ++j) {
-      ok = mbar_wait_bounded(&s_full[g], j & 1, abort_flag, p.err);
+    for (int s = 0; s < c; ++s) {
+      ok = mbar_wait_bounded(&s_full[g], sc & 1, abort_flag, p.err);
+      ++sc;
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int key0 = (j_lo + j) * kBN;
-      const bool need_mask = key0 + kBN - 1 > pos0[g];
+      const int key0 = (j_lo + (split ? 2 * s + g : s)) * kBN;
+      const bool need_mask = key0 + kBN - 1 > p0;
       // One TMEM round trip per tile: all 128 scores of the row are loaded
       // (four loads, one wait), the row max is taken over the raw scores (the
       // scale is positive, so it commutes with the max) with eight independent
       // accumulators, and the probabilities are computed from registers.
       uint32_t x[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32_async(tmem + lane_off + colS + 32 * c, x + 32 * c);
+      for (int q = 0; q < 4; ++q) tmem_ld32_async(tmem + lane_off + colS + 32 * q, x + 32 * q);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_wait_ld32(x + 32 * c);
+      for (int q = 0; q < 4; ++q) tmem_wait_ld32(x + 32 * q);
       if (need_mask) {
 #pragma unroll
         for (int e = 0; e < 128; ++e)
@@ -530,20 +557,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (__any_sync(0xffffffffu, mx > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, mx);
         const float alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
-        if (j > 0) {
-          ok = mbar_wait_bounded(&pv_done[g], (j - 1) & 1, abort_flag, p.err);
+        if (s > 0) {
+          // rescale O_g once the previous PV into it has completed
+          ok = mbar_wait_bounded(&pv_done[g], (pc[g] + s - 1) & 1, abort_flag, p.err);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int q = 0; q < 4; ++q) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + colO + 32 * c, o);
+            tmem_ld32(tmem + lane_off + colO + 32 * q, o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_off + colO + 32 * c, o);
+            tmem_st32(tmem + lane_off + colO + 32 * q, o);
           }
           tmem_wait_st();
         }
@@ -561,12 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float2 t = ffma2(make_float2(__uint_as_float(x[64 * hh + 2 * e]), __uint_as_float(x[64 * hh + 2 * e + 1])),
-                                 make_float2(p.scale_log2, p.scale_log2), make_float2(neg_m, neg_m));
-          const float p0 = ex2(t.x);
-          const float p1 = ex2(t.y);
-          rs4[e & 3] = fadd2(rs4[e & 3], make_float2(p0, p1));
-          w[e] = pack_bf16x2(p0, p1);
+          const float2 tv = ffma2(make_float2(__uint_as_float(x[64 * hh + 2 * e]), __uint_as_float(x[64 * hh + 2 * e + 1])),
+                                  make_float2(p.scale_log2, p.scale_log2), make_float2(neg_m, neg_m));
+          const float p0v = ex2(tv.x);
+          const float p1v = ex2(tv.y);
+          rs4[e & 3] = fadd2(rs4[e & 3], make_float2(p0v, p1v));
+          w[e] = pack_bf16x2(p0v, p1v);
         }
         tmem_st16(tmem + lane_off + colS + 32 * hh, w);
         tmem_st16(tmem + lane_off + colS + 32 * hh + 16, w + 16);
@@ -578,59 +606,533 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[g]);
     }
-    // epilogue: O / l to global memory, or this part's partial result
-    if (g < nq && slot >= 0) {
-      if (ok) ok = mbar_wait_bounded(o_final, 0, abort_flag, p.err);
-      const int64_t prow = ((static_cast<int64_t>(slot) * p.Hkv + h) * 2 + g) * kBM + row;
-      if (__all_sync(0xffffffffu, ok)) {
-        if (ntl[g] > 0) {
-          tc_fence_after();
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          float* dstp = p.o_part + prow * 128;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + colO + 32 * c, o);
+    if (!ok) break;
+    const int last_pv0 = pc[0] + c0 - 1, last_pv1 = pc[1] + c1 - 1;  // running indices
+    pc[0] += c0;
+    pc[1] += c1;
+    const int qt = 2 * it_qp + qtg;  // q-tile index in the request
+    const int64_t prow = ((static_cast<int64_t>(slot) * p.Hkv + hh_kv) * 2 + qtg) * kBM + row;
+    char* dst = p.out + ((static_cast<int64_t>(it_s0) + qt * p.TQ + t_r) * p.Hq + hh_kv * p.G + gg) * 256;
+    if (!split) {
+      // ------------- pair mode epilogue: this group's q-tile -------------
+      if (c > 0) {
+        ok = mbar_wait_bounded(&pv_done[g], (g ? last_pv1 : last_pv0) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // the whole row in one TMEM round trip; O_g is free for the next item
+        // as soon as it is in registers
+        uint32_t o[128];
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              *reinterpret_cast<float4*>(dstp + 32 * c + 4 * q4) =
-                  make_float4(__uint_as_float(o[4 * q4]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
-                              __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
-          }
-          p.lse_part[prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
-        } else {
-          p.lse_part[prow] = -INFINITY;  // no key tile of this part reaches q-tile g
+        for (int q = 0; q < 4; ++q) tmem_ld32_async(tmem + lane_off + colO + 32 * q, o + 32 * q);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_wait_ld32(o + 32 * q);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_free[g]);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        store_cols<0>(o, inv, slot >= 0, live, p.o_part + prow * 128, dst, p.out32);
+        if (slot >= 0) p.lse_part[prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
+      } else if (slot >= 0) {
+        p.lse_part[prow] = -INFINITY;  // no key tile of this part reaches the q-tile
+      }
+    } else if (g == 1) {
+      // ------------- split mode: group 1 hands its row statistics over -------------
+      if (ms > 0) {
+        ok = mbar_wait_bounded(ml_empty, (ms - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
       }
-    } else if (g < nq) {
-      if (ok) ok = mbar_wait_bounded(o_final, 0, abort_flag, p.err);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        char* dst = p.out + ((static_cast<int64_t>(s0) + (2 * qp + g) * p.TQ + t) * p.Hq + h * p.G + gg) * 256;
+      ml[row] = make_float2(m_used, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ml_full);
+      ++ms;
+    } else {
+      // ------------- split mode: group 0 merges both halves of the keys -------------
+      ok = mbar_wait_bounded(&pv_done[0], last_pv0 & 1, abort_flag, p.err) &&
+           mbar_wait_bounded(ml_full, ms & 1, abort_flag, p.err) &&
+           (c1 == 0 || mbar_wait_bounded(&pv_done[1], last_pv1 & 1, abort_flag, p.err));
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float2 m1 = ml[row];
+      const float mm = fmaxf(m_used, m1.x);
+      const float w0 = m_used == -INFINITY ? 0.f : ex2(m_used - mm);
+      const float w1 = m1.x == -INFINITY ? 0.f : ex2(m1.x - mm);
+      const float lsum = w0 * l + w1 * m1.y;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float a0 = w0 * inv, a1 = w1 * inv;
+      const bool two = c1 > 0;
+      // half a row of each O per TMEM round trip (the other group's O only
+      // when it ran: otherwise it holds an earlier item's values)
+      // a quarter row of each O per TMEM round trip (the other group's O only
+      // when it ran: otherwise it holds an earlier item's values)
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + colO + 32 * c, o);
-          if (live) {
+      for (int q = 0; q < 4; ++q) {
+        uint32_t o[32];
+        if (two) {
+          uint32_t o1[32];
+          tmem_ld32_async(tmem + lane_off + 256 + 32 * q, o);
+          tmem_ld32_async(tmem + lane_off + 384 + 32 * q, o1);
+          tmem_wait_ld32(o);
+          tmem_wait_ld32(o1);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + c * 64 + q4 * 16) = w;
+          for (int e = 0; e < 32; ++e)
+            o[e] = __float_as_uint(fmaf(__uint_as_float(o[e]), a0, __uint_as_float(o1[e]) * a1));
+        } else {
+          tmem_ld32(tmem + lane_off + 256 + 32 * q, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a0);
+        }
+        store_cols<0>(o, 1.f, slot >= 0, live, p.o_part + prow * 128 + 32 * q, dst + 64 * q, p.out32);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(ml_empty);
+        mbar_arrive(&o_free[0]);
+        if (two) mbar_arrive(&o_free[1]);
+      }
+      if (slot >= 0) p.lse_part[prow] = lsum > 0.f ? mm + __log2f(lsum) : -INFINITY;
+      ++ms;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (p.units) {
+    pdl_trigger();  // the merge kernel may start launching; it waits for this grid
+  } else {
+    // one pair per CTA: a pair without rows leaves at once (the same for every thread)
+    const int b = blockIdx.z;
+    if (2 * static_cast<int>(blockIdx.x) * p.TQ >= p.cu[b + 1] - p.cu[b]) return;
+  }
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* item_full = bars + kBarItemFull;    // [2] scheduler -> all roles
+  uint64_t* item_empty = bars + kBarItemEmpty;   // [2] all roles -> scheduler
+  uint64_t* q_full = bars + kBarQFull;       // the item's Q tiles landed
+  uint64_t* q_empty = bars + kBarQEmpty;      // the item's last QK is done
+  uint64_t* k_full = bars + kBarKFull;       // [2] K stages
+  uint64_t* k_empty = bars + kBarKEmpty;
+  uint64_t* v_full = bars + kBarVFull;      // [2] V stages
+  uint64_t* v_empty = bars + kBarVEmpty;
+  uint64_t* s_full = bars + kBarSFull;      // [2] per softmax group: S = Q K^T in TMEM
+  uint64_t* p_full = bars + kBarPFull;      // [2] probabilities written
+  uint64_t* pv_done = bars + kBarPvDone;     // [2] a PV of the group completed
+  uint64_t* o_free = bars + kBarOFree;      // [2] O of the group read out by the epilogue
+  uint64_t* ml_full = bars + kBarMlFull;     // group 1's (max, sum) rows handed to group 0
+  uint64_t* ml_empty = bars + kBarMlEmpty;    // group 0 has read them
+  uint64_t* mma_done = bars + kBarMmaDone;    // every MMA of the CTA completed
+  uint64_t* sched_go = bars + kBarSchedGo;    // the current item's K tiles are all issued
+  Item* items = reinterpret_cast<Item*>(smem + kOffItem);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc) + 1;
+
+  // V rows past the last key of a tile meet a probability of 0 in the PV
+  // products, so they must hold finite values: both V stages start zeroed and
+  // the V producer zeroes the rows a ragged tile leaves unloaded.
+  {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += kThreads)
+      reinterpret_cast<uint4*>(smem + kOffV)[i] = z;
+  }
+  fence_async_smem();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&item_full[s], 1);
+      mbar_init(&item_empty[s], kItemConsumers);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&o_free[s], 4);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(ml_full, 4);
+    mbar_init(ml_empty, 4);
+    mbar_init(mma_done, 1);
+    mbar_init(sched_go, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cta_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // Registers: the launch gives every thread kLaunchRegs; the copy, MMA and
+  // scheduler warpgroup hands most of its share to the two softmax
+  // warpgroups (the sum stays within the launch's allocation).
+  if (warp < kKWarp) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    SoftmaxArgs sa;
+    sa.out = p.out;
+    sa.out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+    sa.o_part = p.o_part;
+    sa.lse_part = p.lse_part;
+    sa.err = p.err;
+    sa.Hq = p.Hq;
+    sa.Hkv = p.Hkv;
+    sa.G = p.G;
+    sa.TQ = p.TQ;
+    sa.scale_log2 = p.scale_log2;
+    softmax_role(sa, smem, tmem, warp, lane);
+    tc_fence_before();
+    cta_sync();  // pairs with the other warpgroup's barrier before the TMEM is freed
+    return;
+  }
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRoleRegs));
+  if (warp == kSchedWarp) {
+    // ------------------------------- work scheduler -------------------------------
+    // Planned launch: items k = unit * Hkv + kv-head are taken from a shared
+    // counter, so a CTA that finishes early takes the next one (the units are
+    // listed longest first).  Otherwise the CTA's own pair is its one item.
+    if (lane == 0) {
+      if (p.units) pdl_wait();  // the planner's unit list and counter are ready
+      const int total = p.units ? *p.n_units * p.Hkv : 1;
+      int pub = 0, k_own = 0;
+      for (;;) {
+        Item it;
+        it.valid = 0;
+        // Take the next item only when this CTA is about to need it (its
+        // previous item's K tiles are all issued), so that the items, listed
+        // longest first, go to the CTAs that free up first.
+        if (pub > 0) {
+          const uint64_t tg = global_timer_ns();
+          bool okg = true;
+          while (!mbar_try_wait(sched_go, (pub - 1) & 1)) {
+            __nanosleep(64);
+            if (*abort_flag || global_timer_ns() - tg > kWaitLimitNs) {
+              if (!*abort_flag) raise_flag(p.err, PA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              okg = false;
+              break;
+            }
+          }
+          if (!okg) break;
+        }
+        const int k = p.units ? atomicAdd(p.counter, 1) : k_own++;
+        const bool last = k >= total;
+        if (!last) {
+          int b, qp, h, jl, jh, sl;
+          if (p.units) {
+            const int u = k / p.Hkv;
+            h = k - u * p.Hkv;
+            const int4 ud = p.units[u];
+            b = ud.x;
+            qp = ud.y;
+            jl = ud.z & 0xffff;
+            jh = static_cast<int>(static_cast<uint32_t>(ud.z) >> 16);
+            sl = ud.w;
+          } else {
+            b = blockIdx.z;
+            h = blockIdx.y;
+            qp = blockIdx.x;
+            jl = 0;
+            jh = 1 << 30;
+            sl = -1;
+          }
+          if (!make_item(p, b, qp, h, jl, jh, sl, it)) continue;
+        }
+        const int s = pub & 1;
+        // the slot frees when every role has taken the item two back: poll
+        // slowly, so as not to take issue slots from the softmax warps
+        const uint32_t par = ((pub >> 1) & 1) ^ 1;
+        const uint64_t tw = global_timer_ns();
+        bool okw = true;
+        while (!mbar_try_wait(&item_empty[s], par)) {
+          __nanosleep(500);
+          if (*abort_flag || global_timer_ns() - tw > kWaitLimitNs) {
+            if (!*abort_flag) raise_flag(p.err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            okw = false;
+            break;
+          }
+        }
+        if (!okw) break;
+        items[s] = it;
+        mbar_arrive(&item_full[s]);  // release: the item's fields are visible to its waiters
+        ++pub;
+        if (last) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kKWarp || warp == kVWarp) {
+    // ------------------------------- TMA producers -------------------------------
+    // Warp kKWarp copies each item's Q tiles and its K tiles, warp kVWarp its V
+    // tiles, each into its own two-stage ring that runs on across items.
+    const bool vrole = warp == kVWarp;
+    const int box = lane >> 2, half = (lane >> 1) & 1, isv = lane & 1;
+    uint64_t* full = vrole ? v_full : k_full;
+    uint64_t* empty = vrole ? v_empty : k_empty;
+    const CUtensorMap* m16 = vrole ? &p.tm_v16 : &p.tm_k16;
+    const CUtensorMap* m1 = vrole ? &p.tm_v1 : &p.tm_k1;
+    constexpr int kNoPage = INT_MIN;
+    int kc = 0;  // tiles issued into this ring
+    int nq_issued = 0;  // items whose Q tiles were issued
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      Item it;
+      if (!take_item(items, item_full, item_empty, i, abort_flag, p.err, it)) {
+        ok = false;
+        break;
+      }
+      if (!it.valid) break;
+      const int64_t bt_row = static_cast<int64_t>(it.b) * p.maxp;
+      const int x = it.h * 128 + half * 64;
+      // Block-table entries of tile t: lane `box` reads the page of its 16-row
+      // box, lanes 0-3 the page of a ragged end.
+      auto load_pages = [&](int t, int& pg_full, int& pg_rem) {
+        const int t0 = (it.j_lo + t) * kBN;
+        const int valid = min(kBN, it.kv_len - t0);
+        const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+        pg_full = box < nfull ? p.bt[bt_row + ((t0 + box * kBoxRows) >> p.log2P)] : kNoPage;
+        pg_rem = rem && lane < 4 ? p.bt[bt_row + ((t0 + nfull * kBoxRows) >> p.log2P)] : kNoPage;
+      };
+      int pf_next = kNoPage, pr_next = kNoPage;
+      load_pages(0, pf_next, pr_next);
+      if (!vrole) {
+        // the item's Q tiles, once the previous item's last QK has read Q
+        int okq = 1;
+        if (lane == 0) {
+          okq = i == 0 || mbar_wait_bounded(q_empty, (i - 1) & 1, abort_flag, p.err);
+          if (okq) {
+            ++nq_issued;
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(it.nq * p.G * p.TQ * 256));
+            for (int g = 0; g < it.nq; ++g) {
+              const int z = it.s0 + (2 * it.qp + g) * p.TQ;
+              tma_load_3d(smem + kOffQ + g * kTileBytes, &p.tm_q, 0, it.h * p.G, z, q_full);
+              tma_load_3d(smem + kOffQ + g * kTileBytes + kHalfBytes, &p.tm_q, 64, it.h * p.G, z, q_full);
             }
           }
         }
+        if (!__shfl_sync(0xffffffffu, okq, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      for (int t = 0; t < it.nt; ++t) {
+        const int pf = pf_next, pr = pr_next;
+        if (t + 1 < it.nt) load_pages(t + 1, pf_next, pr_next);  // one tile ahead
+        const int st = kc & 1;
+        const int t0 = (it.j_lo + t) * kBN;
+        const int valid = min(kBN, it.kv_len - t0);
+        const int nfull = valid / kBoxRows, rem = valid % kBoxRows;
+        int y_full = -1, y_rem = -1;
+        if (pf != kNoPage) {
+          if (pf >= 0 && pf < p.num_pages) y_full = (pf << p.log2P) + ((t0 + box * kBoxRows) & (p.P - 1));
+          else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
+        }
+        if (pr != kNoPage) {
+          if (pr >= 0 && pr < p.num_pages) y_rem = (pr << p.log2P) + ((t0 + nfull * kBoxRows) & (p.P - 1));
+          else raise_flag(p.err, PA_DEVERR_BAD_PAGE);
+        }
+        const uint32_t mine = (y_full >= 0 ? kBoxRows * 128 : 0) + (y_rem >= 0 ? rem * 128 : 0);
+        uint32_t bytes = (isv != 0) == vrole ? mine : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait_bounded(&empty[st], ((kc >> 1) & 1) ^ 1, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) {
+          ok = false;
+          break;
+        }
+        unsigned char* stage = smem + (vrole ? kOffV : kOffK) + st * kTileBytes;
+        if (vrole && valid < kBN) {
+          // a ragged tile: zero the rows it leaves unloaded (they may hold
+          // another request's values), before the copies are counted
+          const int chunks = (kBN - valid) * 16;
+          for (int c = lane; c < chunks; c += 32) {
+            const int r = valid + (c >> 4), ch = c & 15;
+            *reinterpret_cast<uint4*>(stage + (ch >> 3) * kHalfBytes + r * 128 + (ch & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+        __syncwarp();
+        if ((isv != 0) == vrole) {
+          unsigned char* dst = stage + half * kHalfBytes;
+          if (y_full >= 0) tma_load_2d(dst + box * kBoxRows * 128, m16, x, y_full, &full[st]);
+          if (y_rem >= 0)
+            for (int r = 0; r < rem; ++r) tma_load_2d(dst + (nfull * kBoxRows + r) * 128, m1, x, y_rem + r, &full[st]);
+        }
+        ++kc;
+      }
+      if (!ok) break;
+      if (!vrole) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sched_go);  // the scheduler may take the next item
       }
     }
+    if (!ok && lane == 0) {
+      // copies may still be landing: wait for them (time only) before the CTA exits
+      if (!vrole && nq_issued > 0) drain(q_full, (nq_issued - 1) & 1);
+      for (int j = max(0, kc - 2); j < kc; ++j) drain(&full[j & 1], (j >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      // low descriptor halves of the two Q tiles and the K / V stages; an MMA's
+      // operand is its tile's plus the address offset >> 4 (the 14-bit address
+      // field never carries: shared addresses are < 256 KB)
+      const uint32_t dQ0 = desc_lo(smem_u32(smem + kOffQ), 16);
+      const uint32_t dQ1 = desc_lo(smem_u32(smem + kOffQ + kTileBytes), 16);
+      const uint32_t dK0 = desc_lo(smem_u32(smem + kOffK), 16);
+      const uint32_t dK1 = desc_lo(smem_u32(smem + kOffK + kTileBytes), 16);
+      const uint32_t dV0 = desc_lo(smem_u32(smem + kOffV), kHalfBytes);
+      const uint32_t dV1 = desc_lo(smem_u32(smem + kOffV + kTileBytes), kHalfBytes);
+      const uint32_t bar0 = smem_u32(bars);
+      int kc = 0;          // K/V tiles consumed before this item (both rings advance alike)
+      int pc0 = 0, pc1 = 0;  // PVs issued per group
+      int ow0 = 0, ow1 = 0;  // items whose O_g has been written
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        Item it;
+        if (!take_item_lane(items, item_full, item_empty, i, abort_flag, p.err, it)) break;
+        if (!it.valid) break;
+        if (!(ok = mbar_wait_bounded(q_full, i & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        const int c0 = it.c[0], c1 = it.c[1];
+        int qk_left = c0 + c1;  // the item's last QK releases the Q tiles
+        // ring stage and phase of the item's tile t
+        auto st_of = [&](int t) { return (kc + t) & 1; };
+        auto ph_of = [&](int t) { return static_cast<uint32_t>(((kc + t) >> 1) & 1); };
+        // barrier i of the table at the top of the kernel
+        auto bar = [&](int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); };
+        auto wait_k = [&](int t) {
+          const bool r = wait_a(bar(kBarKFull + st_of(t)), ph_of(t), abort_flag, p.err);
+          tc_fence_after();
+          return r;
+        };
+        auto wait_v = [&](int t) { return wait_a(bar(kBarVFull + st_of(t)), ph_of(t), abort_flag, p.err); };
+        auto rel_k = [&](int t) { commit_a(bar(kBarKEmpty + st_of(t))); };
+        auto rel_v = [&](int t) { commit_a(bar(kBarVEmpty + st_of(t))); };
+        // S_g = Q K_t^T into TMEM columns g * 128
+        auto qk = [&](int g, uint32_t dq, int t) {
+          issue_qk(tmem + g * 128, dq, st_of(t) ? dK1 : dK0);
+          commit_a(bar(kBarSFull + g));
+          if (--qk_left == 0) commit_a(bar(kBarQEmpty));
+        };
+        // O_g (+)= P_g V_t once the group's probabilities are written; the
+        // item's first PV overwrites O_g after the previous item's epilogue read it
+        auto pv0 = [&](int t, bool first) -> bool {
+          if (!wait_a(bar(kBarPFull), pc0 & 1, abort_flag, p.err)) return false;
+          if (first) {
+            if (ow0 > 0 && !wait_a(bar(kBarOFree), (ow0 - 1) & 1, abort_flag, p.err)) return false;
+            ++ow0;
+          }
+          tc_fence_after();
+          issue_pv(tmem + 256, tmem, st_of(t) ? dV1 : dV0, first);
+          commit_a(bar(kBarPvDone));
+          ++pc0;
+          return true;
+        };
+        auto pv1 = [&](int t, bool first) -> bool {
+          if (!wait_a(bar(kBarPFull + 1), pc1 & 1, abort_flag, p.err)) return false;
+          if (first) {
+            if (ow1 > 0 && !wait_a(bar(kBarOFree + 1), (ow1 - 1) & 1, abort_flag, p.err)) return false;
+            ++ow1;
+          }
+          tc_fence_after();
+          issue_pv(tmem + 384, tmem + 128, st_of(t) ? dV1 : dV0, first);
+          commit_a(bar(kBarPvDone + 1));
+          ++pc1;
+          return true;
+        };
+        // Order per step: PV_0, QK_0 of the next step, PV_1, QK_1 of the next
+        // step -- each softmax group has a PV and a QK of the other group to
+        // hide in, and QK_g overwrites S_g only after PV_g read P_g (one
+        // thread's MMAs execute in issue order).
+        if (!it.split) {
+          // pair mode: tile s feeds q-tile 0 (its first c0 tiles) and q-tile 1 (all c1 = nt)
+          if ((ok = wait_k(0))) {
+            if (c0 > 0) qk(0, dQ0, 0);
+            qk(1, dQ1, 0);
+            rel_k(0);
+          }
+          for (int s = 0; s < c1 && ok; ++s) {
+            const bool more = s + 1 < c1;
+            if (!(ok = wait_v(s))) break;
+            if (s < c0 && !(ok = pv0(s, s == 0))) break;
+            if (more) {
+              if (!(ok = wait_k(s + 1))) break;
+              if (s + 1 < c0) qk(0, dQ0, s + 1);
+            }
+            if (!(ok = pv1(s, s == 0))) break;
+            rel_v(s);
+            if (more) {
+              qk(1, dQ1, s + 1);
+              rel_k(s + 1);
+            }
+          }
+        } else {
+          // split mode: q-tile 0 only; group 0 takes the item's tiles 0, 2, 4, ...,
+          // group 1 tiles 1, 3, 5, ...
+          if ((ok = wait_k(0))) {
+            qk(0, dQ0, 0);
+            rel_k(0);
+          }
+          if (ok && c1 > 0 && (ok = wait_k(1))) {
+            qk(1, dQ0, 1);
+            rel_k(1);
+          }
+          for (int s = 0; s < c0 && ok; ++s) {
+            const int ta = 2 * s, tb = 2 * s + 1;
+            if (!(ok = wait_v(ta))) break;
+            if (!(ok = pv0(ta, s == 0))) break;
+            rel_v(ta);
+            if (s + 1 < c0) {
+              if (!(ok = wait_k(ta + 2))) break;
+              qk(0, dQ0, ta + 2);
+              rel_k(ta + 2);
+            }
+            if (s < c1) {
+              if (!(ok = wait_v(tb))) break;
+              if (!(ok = pv1(tb, s == 0))) break;
+              rel_v(tb);
+              if (s + 1 < c1) {
+                if (!(ok = wait_k(tb + 2))) break;
+                qk(1, dQ0, tb + 2);
+                rel_k(tb + 2);
+              }
+            }
+          }
+        }
+        kc += it.nt;
+      }
+      // every MMA has completed before the tensor memory is freed
+      mma_commit(mma_done);
+      drain(mma_done, 0);
+    }
+    __syncwarp();
   }
 
   tc_fence_before();
   cta_sync();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
@@ -668,10 +1170,10 @@ struct PlanParams {
   const int32_t* cu;
   const int32_t* ctx;
   unsigned int* err;
-  int4* pairs;   // [pair_cap] {request, pair, nt, 0}
+  int4* pairs;   // [pair_cap] {request, pair, nt, q-tiles with rows}
   int4* units;   // [pair_cap + slot_cap]
   int4* splits;  // [split_cap] {request, pair, first slot, parts}
-  int32_t* hdr;  // {units, split pairs, tau, pairs}
+  int32_t* hdr;  // {units, split pairs, tau, pairs, work counter}
   int64_t num_tokens;
   int32_t B, TQ, Hkv, n_sm, max_seqlen_q, cap_ctx, pair_cap, slot_cap, split_cap;
 };
@@ -705,6 +1207,17 @@ PA_DEVINL T block_scan_excl(T v, T* sh, T* total) {
 }
 
 PA_DEVINL int parts_of(int nt, int tau) { return (nt + tau - 1) / tau; }
+
+// Estimated time of a unit of `len` key tiles in steps of the attention
+// kernel (one step: a 128-key tile of a q-tile pair): a single q-tile's key
+// tiles alternate between the two softmax groups and take about 0.7 step
+// each (two new K/V tiles per step); the hand-over between items costs about
+// three steps, a part two more (its fp32 partial result, its share of the
+// merge).
+PA_DEVINL int unit_cost(int len, int nq, int part) {
+  return (nq == 2 ? len : (7 * len + 9) / 10) + 3 + 2 * part;
+}
+PA_DEVINL int cost_bucket(int len, int nq, int part) { return min(unit_cost(len, nq, part), kPlanBuckets - 1); }
 
 // A pair of nt key tiles cut into `parts` ranges: the first nt % parts ranges
 // hold one tile more than the others (lengths base + 1 and base).
@@ -742,7 +1255,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     const unsigned long long off = carry + block_scan_excl<unsigned long long>(np, sh_scan, &tot);
     for (int k = 0; k < np; ++k) {
       const int nt = (L - n + min((2 * k + 2) * q.TQ, n) + kBN - 1) / kBN;
-      const int4 pr = make_int4(b, k, nt, 0);
+      const int4 pr = make_int4(b, k, nt, (2 * k + 1) * q.TQ < n ? 2 : 1);
       if (off + k < static_cast<unsigned long long>(q.pair_cap)) q.pairs[off + k] = pr;
       if (off + k < kPlanSmemPairs) sh_pairs[off + k] = pr;
       max_nt = max(max_nt, nt);
@@ -753,7 +1266,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
   if (carry > static_cast<unsigned long long>(q.pair_cap)) {  // lengths disagree with the workspace's sizes
     if (tid == 0) {
       raise_flag(q.err, PA_DEVERR_BAD_LENGTH);
-      q.hdr[0] = q.hdr[1] = q.hdr[2] = q.hdr[3] = 0;
+      q.hdr[0] = q.hdr[1] = q.hdr[2] = q.hdr[3] = q.hdr[4] = 0;
     }
     return;
   }
@@ -774,13 +1287,15 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
                           : max(2, static_cast<int>(ceilf(max_nt * exp2f(-log2f(0.5f * max_nt) * c / (n_cand - 1)))));
       int units = 0, slots = 0, work = 0, cmax = 0;
       for (int i = lane; i < n_pairs; i += 32) {
-        const int nt = pair_at(i).z;
+        const int4 pr = pair_at(i);
+        const int nt = pr.z, nq = pr.w;
         const int parts = parts_of(nt, t_c);
         const int split = parts > 1;
+        const int base = nt / parts, rem = nt - base * parts;
         units += parts;
         slots += split ? parts : 0;
-        work += nt + parts * (1 + split);
-        cmax = max(cmax, (nt + parts - 1) / parts + 1 + split);
+        work += rem * unit_cost(base + 1, nq, split) + (parts - rem) * unit_cost(base, nq, split);
+        cmax = max(cmax, unit_cost(rem ? base + 1 : base, nq, split));
       }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
@@ -817,12 +1332,13 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     tau = sh_tau;
   }
 
-  // 3. histogram of unit lengths, then bucket cursors in descending length order
+  // 3. histogram of unit costs, then bucket cursors in descending cost order
   for (int i = tid; i < n_pairs; i += kPlanThreads) {
-    const int nt = pair_at(i).z;
-    const int parts = parts_of(nt, tau), base = nt / parts, rem = nt - base * parts;
-    if (rem) atomicAdd(&cursor[min(base + 1, kPlanBuckets - 1)], rem);
-    if (parts > rem) atomicAdd(&cursor[min(base, kPlanBuckets - 1)], parts - rem);
+    const int4 pr = pair_at(i);
+    const int nt = pr.z, nq = pr.w;
+    const int parts = parts_of(nt, tau), base = nt / parts, rem = nt - base * parts, split = parts > 1;
+    if (rem) atomicAdd(&cursor[cost_bucket(base + 1, nq, split)], rem);
+    if (parts > rem) atomicAdd(&cursor[cost_bucket(base, nq, split)], parts - rem);
   }
   cta_sync();
   {
@@ -856,8 +1372,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     if (parts > 0) {
       const int slot0 = static_cast<int>((before >> 32) & 0xffff), si = static_cast<int>(before >> 48);
       const int base = pr.z / parts, rem = pr.z - base * parts;
-      const int p_hi = rem ? atomicAdd(&cursor[min(base + 1, kPlanBuckets - 1)], rem) : 0;
-      const int p_lo = parts > rem ? atomicAdd(&cursor[min(base, kPlanBuckets - 1)], parts - rem) : 0;
+      const int p_hi = rem ? atomicAdd(&cursor[cost_bucket(base + 1, pr.w, split)], rem) : 0;
+      const int p_lo = parts > rem ? atomicAdd(&cursor[cost_bucket(base, pr.w, split)], parts - rem) : 0;
       for (int k = 0; k < parts; ++k) {
         const int j0 = k * base + min(k, rem);
         const int j1 = j0 + base + (k < rem);
@@ -873,6 +1389,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     q.hdr[1] = static_cast<int>(acc >> 48);
     q.hdr[2] = tau;
     q.hdr[3] = n_pairs;
+    q.hdr[4] = 0;  // the attention kernel's work counter
   }
 }
 
@@ -1078,6 +1595,13 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
     std::lock_guard<std::mutex> lk(mu);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!done[dev]) {
+      // The warpgroups' register rebalance assumes the launch allocation; a
+      // build with another register count would make the softmax warpgroups
+      // wait for registers that are never released, so it is not launched.
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
       e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
       done[dev] = true;
@@ -1119,14 +1643,17 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
 
   p.units = q.units;
   p.n_units = q.hdr;
+  p.counter = q.hdr + 4;
   p.lse_part = reinterpret_cast<float*>(ws + pl.off_lse);
   p.o_part = reinterpret_cast<float*>(ws + pl.off_o);
   {
+    // persistent: one CTA per SM (at most one per possible item), each taking
+    // items until the list is exhausted
+    const int64_t items = static_cast<int64_t>(pl.pair_cap + pl.run_slot_cap) * d.num_kv_heads;
+    const unsigned ctas = static_cast<unsigned>(std::min<int64_t>(pl.n_sm, items));
     void* args[] = {&p};
-    e = launch_after_previous(reinterpret_cast<const void*>(prefill_tc_kernel),
-                              dim3(static_cast<unsigned>(pl.pair_cap + pl.run_slot_cap) * d.num_kv_heads),
-                              dim3(kThreads), kSmemBytes, s,
-                              args);
+    e = launch_after_previous(reinterpret_cast<const void*>(prefill_tc_kernel), dim3(ctas), dim3(kThreads),
+                              kSmemBytes, s, args);
     if (e != cudaSuccess) return e;
   }
 
