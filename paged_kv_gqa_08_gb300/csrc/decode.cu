@@ -17,16 +17,24 @@
 //     chunk's K and V rows into a 3-stage shared-memory ring, with mbarrier
 //     completion and an evict-first L2 hint.  Its 32 lanes look up block-table
 //     entries for 32 chunks at a time.
-//   * One consumer warp per kv-head reads its head's rows of the chunk: each
-//     lane owns 16 bytes of a row, so one K/V byte feeds all G q-heads of the
-//     group from registers.  Dot products use packed fp32x2 FMA; partial sums
-//     are reduced with a halving butterfly of warp shuffles; the online
-//     softmax runs in base 2 with the scale folded into q.
+//   * One consumer warp per kv-head reads its head's rows of the chunk, so
+//     one K/V byte feeds all G q-heads of the group.  Two consumers:
+//     - CUDA cores (fp32, head_dim 64, groups of up to 3): each lane owns 16
+//       bytes of a row; dot products use packed fp32x2 FMA, partial sums are
+//       reduced with a halving butterfly of warp shuffles, the online
+//       softmax runs in base 2 with the scale folded into q.
+//     - tensor cores (bf16, head_dim 128, groups of 4 to 8): per 16-token
+//       chunk, S = Q K^T and O += P V as mma.sync m16n8k16 with the group's
+//       q-heads as the (zero-padded) 16 rows; K and V fragments come by
+//       ldmatrix from stage rows padded by 16 bytes (each row its own copy),
+//       so the loads are free of bank conflicts.  Far fewer instructions per
+//       byte: the CUDA-core consumer is issue-bound at G = 4.
 //   * Every wait is bounded (pa::mbar_wait_bounded): a kernel never hangs.
 #include <math.h>
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "pa_common.cuh"
 
@@ -34,7 +42,9 @@ namespace pa {
 namespace {
 
 constexpr int kTPL = 4;          // tokens per lane per chunk
-constexpr int kStages = 3;       // shared-memory ring depth
+constexpr int kStages = 3;       // shared-memory ring depth (CUDA-core consumers, up to two CTAs per SM)
+constexpr int kStagesMma = 3;    // ring depth of the tensor-core consumers (one CTA per SM)
+constexpr int kMmaTok = 16;      // tokens per chunk of the tensor-core consumers
 constexpr int kPlanThreads = 1024;
 constexpr int kMergeThreads = 128;
 
@@ -68,7 +78,8 @@ struct KParams {
   int32_t B, Hq, Hkv, P, maxp, max_ctx, n_ctas;
   int32_t log2P, log2T;
   int32_t row_bytes;    // Hkv * HD * E, one token of the cache
-  int32_t chunk_bytes;  // T * row_bytes
+  int32_t row_pitch;    // shared-memory bytes per token row of a stage (row_bytes, + 16 for the MMA consumers)
+  int32_t chunk_bytes;  // T * row_pitch
   uint32_t off_bar, off_meta, off_p, off_alpha, off_ml, off_abort;
   int32_t p_row;        // floats per token row of the probability tile
   float scale_log2;     // softmax scale * log2(e)
@@ -235,12 +246,198 @@ PA_DEVINL void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
+// tensor-core consumer (bf16, head_dim 128, G >= 4 q-heads per kv-head)
+// ---------------------------------------------------------------------------
+// mma.sync fragments (PTX ISA, m16n8k16 with .row.col): lane l is
+// in row group gq = l / 4 and thread-in-group tq = l % 4.  A holds rows gq and
+// gq + 8; B holds column gq; C holds rows gq (c0, c1) and gq + 8 (c2, c3) at
+// columns 2 tq, 2 tq + 1.  Here the rows are the group's q-heads (G <= 8 of
+// them, padded to 16 with zero rows), so only c0 / c1 of lanes with gq < G
+// carry results.
+PA_DEVINL void mma_16816(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  [[maybe_unused]] float x2, x3;  // rows gq + 8 (padding), discarded
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %10, %10};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// 2^x on the special-function unit (PTX ex2.approx; x <= 0 here).
+PA_DEVINL float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+
+// Four 8x8 b16 matrices from shared memory; lanes 8i .. 8i+7 give the row
+// addresses of matrix i.  .trans delivers each matrix transposed.
+PA_DEVINL void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+PA_DEVINL void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// The consumer warp of kv-head `warp` for the chunks [x0, x1) of CTA c: per
+// 16-token chunk, S = Q K^T as 16 m16n8k16 MMAs in two chains (K^T fragments
+// by ldmatrix from the padded stage rows), the online softmax in base 2 on
+// the S fragments, and O += P V as 16 m16n8k16 MMAs (P straight from the S
+// fragments, V fragments by transposed ldmatrix).  Same results contract as the CUDA-core
+// consumer: whole requests to `out`, shares to the partial slots.
+template <int G, int NS>
+PA_DEVINL void mma_consumer(const KParams& p, unsigned char* smem, uint64_t* full, uint64_t* empty, const int4* meta,
+                            volatile int* abort_flag, int x0, int x1, int c) {
+  constexpr int RB = 256;  // bytes of one head row (128 bf16)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = warp;
+  const int gq = lane >> 2, tq = lane & 3;
+  const bool row_live = gq < G;
+  const int lrow = lane & 7, lmat = lane >> 3;  // ldmatrix: this lane's row and matrix
+  const uint32_t smem0 = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  uint32_t qa[8][2];  // A fragments of q for k-steps of 16 dims: dims 2tq.. and 2tq+8.. of row gq
+  float o[16][2];     // O row gq, columns 8j + 2tq, 8j + 2tq + 1
+  float m_run = -INFINITY, l_part = 0.f;
+  int b = 0;
+
+  for (int x = x0, it = 0; x < x1; ++x, ++it) {
+    const int s = it % NS;
+    if (!mbar_wait_bounded(&full[s], (it / NS) & 1, abort_flag, p.err)) break;
+    const int4 md = meta[s];
+    b = md.x;
+    const int n = md.y, flags = md.z;
+
+    if (flags & 1) {  // first chunk of this CTA's share of request b
+      const char* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + h * G + (row_live ? gq : 0)) * RB;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qa[ks][0] = row_live ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 2 * tq) * 2) : 0u;
+        qa[ks][1] = row_live ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 8 + 2 * tq) * 2) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = 0.f;
+      m_run = -INFINITY;
+      l_part = 0.f;
+    }
+
+    unsigned char* kst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes + h * RB;
+    unsigned char* vst = kst + p.chunk_bytes;
+    if (md.w >= 0) {
+      // fused KV write: this head's piece of the new row (row n - 1) goes to its slot
+      const int64_t dst_off = static_cast<int64_t>(md.w) * p.row_bytes + h * RB;
+      const unsigned char* src = (lane < 16 ? kst : vst) + (n - 1) * p.row_pitch + (lane & 15) * 16;
+      char* dst = const_cast<char*>(lane < 16 ? p.k_cache : p.v_cache) + dst_off + (lane & 15) * 16;
+      stg16(dst, *reinterpret_cast<const uint4*>(src));
+    }
+    if (n < kMmaTok) {
+      // a ragged chunk: the V rows past its end meet probability 0 and must be
+      // finite (they may hold another chunk's data or nothing yet); the fence
+      // orders these stores before the copies that refill the stage later
+      for (int r = n; r < kMmaTok; ++r)
+        if (lane < 16) *reinterpret_cast<uint4*>(vst + r * p.row_pitch + lane * 16) = make_uint4(0, 0, 0, 0);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+
+    // S = Q K^T for the chunk's tokens 0-7 (s0) and 8-15 (s1): row gq, tokens
+    // 2tq, 2tq + 1 (+ 8); two independent accumulator chains
+    const uint32_t ka = smem0 + static_cast<uint32_t>(kst - smem) + lrow * p.row_pitch + lmat * 16;
+    const uint32_t ka8 = ka + 8 * p.row_pitch;
+    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t bf[4], bg[4];
+      ldsm_x4(bf, ka + kk * 64);
+      ldsm_x4(bg, ka8 + kk * 64);
+      mma_16816(s0, qa[2 * kk][0], qa[2 * kk][1], bf[0], bf[1]);
+      mma_16816(s1, qa[2 * kk][0], qa[2 * kk][1], bg[0], bg[1]);
+      mma_16816(s0, qa[2 * kk + 1][0], qa[2 * kk + 1][1], bf[2], bf[3]);
+      mma_16816(s1, qa[2 * kk + 1][0], qa[2 * kk + 1][1], bg[2], bg[3]);
+    }
+    const int tk = 2 * tq;
+    const float v0 = tk < n ? s0[0] * p.scale_log2 : -INFINITY;
+    const float v1 = tk + 1 < n ? s0[1] * p.scale_log2 : -INFINITY;
+    const float v2 = tk + 8 < n ? s1[0] * p.scale_log2 : -INFINITY;
+    const float v3 = tk + 9 < n ? s1[1] * p.scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = ex2_approx(m_run - m_use);
+    const float p0 = ex2_approx(v0 - m_use), p1 = ex2_approx(v1 - m_use);
+    const float p2 = ex2_approx(v2 - m_use), p3 = ex2_approx(v3 - m_use);
+    l_part = l_part * alpha + ((p0 + p1) + (p2 + p3));
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] *= alpha;
+        o[j][1] *= alpha;
+      }
+    }
+    m_run = m_new;
+
+    // O += P V (m16n8k16: k = the chunk's 16 tokens); matrices of the
+    // transposed loads: tokens 0-7 / 8-15 x dims d .. d+7 / d+8 .. d+15
+    const uint32_t pa0 = pack_bf16x2(p0, p1), pa2 = pack_bf16x2(p2, p3);
+    const uint32_t va = smem0 + static_cast<uint32_t>(vst - smem) + (lrow + (lmat & 1) * 8) * p.row_pitch +
+                        (lmat >> 1) * 16;
+#pragma unroll
+    for (int nn = 0; nn < 8; ++nn) {
+      uint32_t bf[4];
+      ldsm_x4_t(bf, va + nn * 32);
+      mma_16816(o[2 * nn], pa0, pa2, bf[0], bf[1]);
+      mma_16816(o[2 * nn + 1], pa0, pa2, bf[2], bf[3]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    if (flags & 2) {  // last chunk of the share: write the result
+      float l = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (row_live) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int hq = h * G + gq;
+        if (flags & 4) {
+          char* dst = p.out + (static_cast<int64_t>(b) * p.Hq + hq) * RB + tq * 4;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<uint32_t*>(dst + j * 16) = pack_bf16x2(o[j][0] * inv, o[j][1] * inv);
+        } else {
+          const int64_t slot = static_cast<int64_t>(c) + b;
+          float* dst = p.o_part + (slot * p.Hq + hq) * 128 + 2 * tq;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) *reinterpret_cast<float2*>(dst + 8 * j) = make_float2(o[j][0] * inv, o[j][1] * inv);
+          if (tq == 0) p.lse_part[slot * p.Hq + hq] = l > 0.f ? m_run + log2f(l) : -INFINITY;
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // the split-KV decode kernel
 // ---------------------------------------------------------------------------
+// The bf16 head_dim-128 kernels for groups of 4 or more q-heads per kv-head run
+// their products on the tensor cores (see the MMA consumer below).
+template <typename T, int HD, int G>
+constexpr bool kUseMma = std::is_same<T, __nv_bfloat16>::value && HD == 128 && G >= 4;
+
 template <typename T, int HD, int G>
 // Register cap: a 9-warp CTA is charged as 10 warps, so two CTAs per SM need
-// at most 96 registers per thread (G <= 4); larger groups run one CTA per SM.
-__global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_kernel(const KParams p) {
+// at most 96 registers per thread (CUDA-core consumers, G <= 4); larger groups
+// and the tensor-core consumers run one CTA per SM with a deeper ring.
+__global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD, G>) ? 96 : 168)
+    decode_kernel(const KParams p) {
+  constexpr bool kMma = kUseMma<T, HD, G>;
+  constexpr int kStages = kMma ? kStagesMma : ::pa::kStages;
   using Gm = Geom<T, HD>;
   constexpr int LPR = Gm::LPR, RPI = Gm::RPI, NPR = Gm::NPR;
   constexpr int V = G * kTPL;
@@ -329,7 +526,10 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
             const uint32_t bytes = static_cast<uint32_t>(un) * static_cast<uint32_t>(p.row_bytes);
             mbar_arrive_expect_tx(&full[s], 2 * bytes);
             unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
-            if (uslot >= 0) {
+            if constexpr (kMma) {
+              // the row copies are issued by the whole warp below
+              if (uslot >= 0 && p.slot_out) p.slot_out[ub] = uslot;
+            } else if (uslot >= 0) {
               // the cached rows of the chunk, then the new token's row from k_new / v_new
               const uint32_t cached = bytes - p.row_bytes;
               if (cached) {
@@ -352,6 +552,26 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
           aborted = true;
           break;
         }
+        if constexpr (kMma) {
+          // one copy per token row into rows of row_pitch bytes (the pad keeps
+          // the MMA consumers' fragment loads free of bank conflicts): lane r
+          // copies K row r, lane 16 + r V row r; the new token's row comes
+          // from k_new / v_new
+          __syncwarp();
+          const int s = (xg - x0 + u) % kStages;
+          unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
+          const int r = lane & 15;
+          const bool isv = lane >= 16;
+          if (r < un) {
+            unsigned char* d = dst + (isv ? p.chunk_bytes : 0) + r * p.row_pitch;
+            if (uslot >= 0 && r == un - 1) {
+              bulk_g2s(d, isv ? p.v_new + ub * p.v_new_stride : p.k_new + ub * p.k_new_stride, p.row_bytes, &full[s]);
+            } else {
+              const char* src = (isv ? p.v_cache : p.k_cache) + uoff + static_cast<int64_t>(r) * p.row_bytes;
+              bulk_g2s_hint(d, src, p.row_bytes, &full[s], pol);
+            }
+          }
+        }
       }
     }
     if (aborted && lane == 0) {
@@ -363,6 +583,10 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
   }
 
   // ------------------------------- consumers -------------------------------
+  if constexpr (kMma) {
+    mma_consumer<G, kStages>(p, smem, full, empty, meta, abort_flag, x0, x1, c);
+    return;
+  }
   const int h = warp;
   const int rs = lane / LPR, j = lane % LPR;
   const int vbase = (j >> DUP) * VF;
@@ -406,7 +630,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
       // fused KV write: this head's 16-byte pieces of the new row go to its slot
       // (row slots of the warp take K and V in turn)
       const int64_t dst_off = static_cast<int64_t>(md.w) * p.row_bytes + h * Gm::RB + j * 16;
-      const int src_off = (n - 1) * p.row_bytes;
+      const int src_off = (n - 1) * p.row_pitch;
       for (int part = rs; part < 2; part += RPI) {
         const unsigned char* src = (part == 0 ? kbuf : vbuf) + src_off;
         char* dst = const_cast<char*>(part == 0 ? p.k_cache : p.v_cache) + dst_off;
@@ -424,7 +648,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
     for (int i = 0; i < kTPL; ++i) {
       const int t = i * RPI + rs;
       float2 kf[NPR];
-      unpack16<T, NPR>(*reinterpret_cast<const uint4*>(kbuf + t * p.row_bytes), kf);
+      unpack16<T, NPR>(*reinterpret_cast<const uint4*>(kbuf + t * p.row_pitch), kf);
       float b[GP];
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
@@ -496,7 +720,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__(G <= 4 ? 96 : 168) decode_
       const int t = i * RPI + rs;
       if (t < n) {
         float2 vf[NPR];
-        unpack16<T, NPR>(*reinterpret_cast<const uint4*>(vbuf + t * p.row_bytes), vf);
+        unpack16<T, NPR>(*reinterpret_cast<const uint4*>(vbuf + t * p.row_pitch), vf);
         const float4* prow = reinterpret_cast<const float4*>(p_tile + t * PR);
 #pragma unroll
         for (int g2 = 0; g2 < G; g2 += 2) {
@@ -748,6 +972,8 @@ cudaError_t ctas_per_sm(const DeviceInfo& di, const void* fn, int threads, size_
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+bool uses_mma(int dtype, int hd, int G) { return dtype == PA_BF16 && hd == 128 && G >= 4; }
+
 }  // namespace
 
 cudaError_t plan_decode(const pa_cache_desc& d, int batch, int max_ctx, int max_ctas, DecodePlan* out) {
@@ -761,15 +987,17 @@ cudaError_t plan_decode(const pa_cache_desc& d, int batch, int max_ctx, int max_
   const int dpl = 16 / E, lpr = d.head_dim / dpl, rpi = 32 / lpr;
   DecodePlan pl;
   pl.nw = d.num_kv_heads;
-  pl.tokens_per_chunk = kTPL * rpi;
+  pl.tokens_per_chunk = uses_mma(d.dtype, d.head_dim, G) ? kMmaTok : kTPL * rpi;
   const int row_bytes = d.num_kv_heads * d.head_dim * E;
-  pl.chunk_bytes = pl.tokens_per_chunk * row_bytes;
-  pl.stages = kStages;
-  size_t off = static_cast<size_t>(kStages) * 2 * pl.chunk_bytes;
+  pl.row_pitch = uses_mma(d.dtype, d.head_dim, G) ? row_bytes + 16 : row_bytes;
+  pl.chunk_bytes = pl.tokens_per_chunk * pl.row_pitch;
+  const int stages = uses_mma(d.dtype, d.head_dim, G) ? kStagesMma : kStages;
+  pl.stages = stages;
+  size_t off = static_cast<size_t>(stages) * 2 * pl.chunk_bytes;
   pl.off_bar = static_cast<uint32_t>(off);
-  off += 2 * kStages * sizeof(uint64_t);
+  off += 2 * stages * sizeof(uint64_t);
   pl.off_meta = static_cast<uint32_t>(align_up(off, 16));
-  off = pl.off_meta + kStages * 16;
+  off = pl.off_meta + stages * 16;
   pl.off_abort = static_cast<uint32_t>(off);
   off += 16;
   pl.p_row = p_row_floats(G);
@@ -836,6 +1064,7 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   p.log2T = 0;
   while ((1 << p.log2T) < pl.tokens_per_chunk) ++p.log2T;
   p.row_bytes = d.num_kv_heads * d.head_dim * elem_bytes(d.dtype);
+  p.row_pitch = pl.row_pitch;
   p.chunk_bytes = pl.chunk_bytes;
   p.off_bar = pl.off_bar;
   p.off_meta = pl.off_meta;

@@ -95,6 +95,7 @@ struct DecodePlan {
   int nw = 0;            // consumer warps per CTA (= num_kv_heads)
   int tokens_per_chunk = 0;
   int chunk_bytes = 0;   // K (or V) bytes of one chunk in shared memory
+  int row_pitch = 0;     // shared-memory bytes per token row of a chunk
   int stages = 0;
   int n_ctas = 0;        // partitions of the key space
   size_t smem_bytes = 0;
