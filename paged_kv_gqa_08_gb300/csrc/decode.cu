@@ -19,16 +19,16 @@
 //     entries for 32 chunks at a time.
 //   * One consumer warp per kv-head reads its head's rows of the chunk, so
 //     one K/V byte feeds all G q-heads of the group.  Two consumers:
-//     - CUDA cores (fp32, head_dim 64, groups of up to 3): each lane owns 16
+//     - CUDA cores (fp32, or head_dim 64): each lane owns 16
 //       bytes of a row; dot products use packed fp32x2 FMA, partial sums are
 //       reduced with a halving butterfly of warp shuffles, the online
 //       softmax runs in base 2 with the scale folded into q.
-//     - tensor cores (bf16, head_dim 128, groups of 4 to 8): per 16-token
+//     - tensor cores (bf16, head_dim 128, any group of up to 8): per 16-token
 //       chunk, S = Q K^T and O += P V as mma.sync m16n8k16 with the group's
 //       q-heads as the (zero-padded) 16 rows; K and V fragments come by
 //       ldmatrix from stage rows padded by 16 bytes (each row its own copy),
 //       so the loads are free of bank conflicts.  Far fewer instructions per
-//       byte: the CUDA-core consumer is issue-bound at G = 4.
+//       byte: the CUDA-core consumer is issue-bound from G = 4 on.
 //   * Every wait is bounded (pa::mbar_wait_bounded): a kernel never hangs.
 #include <math.h>
 
@@ -246,7 +246,7 @@ PA_DEVINL void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-// tensor-core consumer (bf16, head_dim 128, G >= 4 q-heads per kv-head)
+// tensor-core consumer (bf16, head_dim 128, up to 8 q-heads per kv-head)
 // ---------------------------------------------------------------------------
 // mma.sync fragments (PTX ISA, m16n8k16 with .row.col): lane l is
 // in row group gq = l / 4 and thread-in-group tq = l % 4.  A holds rows gq and
@@ -425,10 +425,10 @@ PA_DEVINL void mma_consumer(const KParams& p, unsigned char* smem, uint64_t* ful
 // ---------------------------------------------------------------------------
 // the split-KV decode kernel
 // ---------------------------------------------------------------------------
-// The bf16 head_dim-128 kernels for groups of 4 or more q-heads per kv-head run
-// their products on the tensor cores (see the MMA consumer below).
+// The bf16 head_dim-128 kernels run their products on the tensor cores (see
+// the MMA consumer below); fp32 and head_dim 64 on the CUDA cores.
 template <typename T, int HD, int G>
-constexpr bool kUseMma = std::is_same<T, __nv_bfloat16>::value && HD == 128 && G >= 4;
+constexpr bool kUseMma = std::is_same<T, __nv_bfloat16>::value && HD == 128;
 
 template <typename T, int HD, int G>
 // Register cap: a 9-warp CTA is charged as 10 warps, so two CTAs per SM need
@@ -972,7 +972,7 @@ cudaError_t ctas_per_sm(const DeviceInfo& di, const void* fn, int threads, size_
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool uses_mma(int dtype, int hd, int G) { return dtype == PA_BF16 && hd == 128 && G >= 4; }
+bool uses_mma(int dtype, int hd, int /*G*/) { return dtype == PA_BF16 && hd == 128; }
 
 }  // namespace
 
