@@ -225,8 +225,11 @@ pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int
   p.eps = eps;
   p.hq = desc->num_q_heads;
   p.hkv = desc->num_kv_heads;
-  for (int i = 0; i < desc->head_dim / 2; ++i)
-    p.inv_freq[i] = pow(static_cast<double>(rope_theta), -2.0 * i / desc->head_dim);
+  for (int i = 0; i < desc->head_dim / 2; ++i) {
+    const double f = pow(static_cast<double>(rope_theta), -2.0 * i / desc->head_dim);
+    p.inv_freq_hi[i] = static_cast<float>(f);
+    p.inv_freq_lo[i] = static_cast<float>(f - static_cast<double>(p.inv_freq_hi[i]));
+  }
   cudaError_t e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }

@@ -110,121 +110,202 @@ struct Vec4<__nv_bfloat16> {
   }
 };
 
-// 2*pi split into a double and the double nearest to the remainder.
-constexpr double kTwoPiHi = 6.283185307179586;
-constexpr double kTwoPiLo = 2.4492935982947064e-16;
+// 2*pi as the float nearest to it plus the float nearest to the remainder
+// (Cody and Waite's additive reduction, 1980), and the float nearest to 1/(2*pi).
+constexpr float kTwoPiF1 = 6.28318548202514648f;
+constexpr float kTwoPiF2 = -1.74845553146951609e-7f;
+constexpr float kInvTwoPiF = 0.159154943091895336f;
 
+// The rotation angle pos * f reduced into [-pi, pi], with f given as the float
+// pair fh + fl.  pos * fh is split exactly into p1 + e1 (an FMA recovers the
+// product's rounding error: Dekker's two-product); pos * fl is below 2^-24 of
+// the angle, so one rounding of it is negligible.  The angle is then reduced
+// by k = rint(pos * fh / (2 pi)) against the two-float 2 pi: each FMA's result
+// is exact or within an ulp of a value below pi, so for angles up to ~2^17 rad
+// (positions up to ~131k at frequency 1) the reduced angle is within a few
+// 1e-7 rad of the exact one.
+PA_DEVINL float reduce_angle(int pos, float fh, float fl) {
+  const float pf = static_cast<float>(pos);  // exact below 2^24
+  const float p1 = pf * fh;
+  const float e1 = fmaf(pf, fh, -p1);
+  const float e2 = pf * fl;
+  const float k = rintf(p1 * kInvTwoPiF);
+  const float r = fmaf(-k, kTwoPiF2, fmaf(-k, kTwoPiF1, p1));
+  return r + (e1 + e2);
+}
+
+constexpr int kNrThreads = 128;
+constexpr int kNrCtasPerSm = 8;
+
+// Shared-memory bytes of one token's stage: its q, k and v rows.
+__host__ __device__ constexpr int nr_stage_bytes(int hq, int hkv, int hd, int e) { return (hq + 2 * hkv) * hd * e; }
+
+// A CTA walks the tokens t = blockIdx.x, blockIdx.x + gridDim.x, ...: one
+// thread copies each token's q, k and v rows into a two-stage shared-memory
+// ring with bulk async copies (TMA engine), two tokens ahead, so the rows of
+// the next token stream in while the current one is normed and rotated.
+// A group of LPH lanes handles one head: lane l owns elements [4l, 4l+4) of
+// the first half and the same of the second half, so each lane holds both
+// members of its rotation pairs.  Values are rounded to the storage type
+// after the normalisation, after the weight and after the rotation (the
+// casts of the Qwen3 norm and rotary in the nano-vLLM learning note); for
+// bf16 the element arithmetic runs on fp32 pairs (packed multiplies and FMAs,
+// one two-lane conversion per rounding).
 template <typename T, int HD>
-__global__ void __launch_bounds__(128) norm_rope_kv_write_kernel(const NormRopeParams p) {
+__global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const NormRopeParams p) {
   constexpr int E = sizeof(T);
   constexpr int PE = 4;
   constexpr int LPH = HD / (2 * PE);  // lanes per head
   constexpr int HPW = 32 / LPH;       // heads per warp pass
-  const int64_t t = blockIdx.x;
+  extern __shared__ __align__(128) unsigned char nr_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / LPH, l = lane % LPH;
-  const int pos = p.positions[t];
-  const int64_t slot = p.slots[t];
-  const bool slot_ok = slot >= 0 && slot < p.num_slots;
-  if (!slot_ok && slot != -1 && threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_SLOT);
+  const int row_q = p.hq * HD * E, row_kv = p.hkv * HD * E;
+  const int stage_bytes = row_q + 2 * row_kv;
+  unsigned char* stages = nr_smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(nr_smem + 2 * stage_bytes);
+  float* cs_s = reinterpret_cast<float*>(full + 2);   // [HD / 2]
+  float* sn_s = cs_s + HD / 2;
+  __shared__ int abort_flag;
 
-  // cos / sin of the token's HD/2 pair indices, once per token (one thread
-  // per pair; fp64 is slow on this GPU, so it is not repeated per lane): the
-  // angle pos * theta^(-2i/HD) is formed and reduced modulo 2*pi in double,
-  // then evaluated in float.
-  __shared__ float cs_s[HD / 2], sn_s[HD / 2];
-  if (threadIdx.x < HD / 2) {
-    const double ang = static_cast<double>(pos) * p.inv_freq[threadIdx.x];
-    const double k = rint(ang * (1.0 / kTwoPiHi));
-    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
-    float sv, cv;
-    sincosf(static_cast<float>(r), &sv, &cv);
-    cs_s[threadIdx.x] = cv;
-    sn_s[threadIdx.x] = sv;
+  const int64_t t0 = blockIdx.x, dt = gridDim.x;
+  const int n_mine = static_cast<int>((p.n_tokens - t0 + dt - 1) / dt);  // tokens of this CTA
+  auto issue = [&](int i) {  // thread 0: the copies of the CTA's i-th token into stage i & 1
+    const int64_t t = t0 + i * dt;
+    unsigned char* st = stages + (i & 1) * stage_bytes;
+    mbar_arrive_expect_tx(&full[i & 1], static_cast<uint32_t>(stage_bytes));
+    bulk_g2s(st, static_cast<const char*>(p.q) + t * p.q_stride * E, row_q, &full[i & 1]);
+    bulk_g2s(st + row_q, static_cast<const char*>(p.k) + t * p.k_stride * E, row_kv, &full[i & 1]);
+    bulk_g2s(st + row_q + row_kv, static_cast<const char*>(p.v) + t * p.v_stride * E, row_kv, &full[i & 1]);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    if (n_mine > 0) issue(0);
+    if (n_mine > 1) issue(1);
   }
-  cta_sync();
-  float cs[PE], sn[PE], nsn[PE];
-#pragma unroll
-  for (int e = 0; e < PE; ++e) {
-    cs[e] = cs_s[l * PE + e];
-    sn[e] = sn_s[l * PE + e];
-    nsn[e] = -sn[e];
-  }
+
   float wq_a[PE], wq_b[PE], wk_a[PE], wk_b[PE];
   Vec4<T>::load(static_cast<const T*>(p.wq) + l * PE, wq_a);
   Vec4<T>::load(static_cast<const T*>(p.wq) + HD / 2 + l * PE, wq_b);
   Vec4<T>::load(static_cast<const T*>(p.wk) + l * PE, wk_a);
   Vec4<T>::load(static_cast<const T*>(p.wk) + HD / 2 + l * PE, wk_b);
+  int pos_next = n_mine > 0 ? p.positions[t0] : 0;
+  int64_t slot_next = n_mine > 0 ? p.slots[t0] : -1;
+  cta_sync();
 
-  const int nheads = p.hq + p.hkv;
-  for (int hh = warp * HPW + sub; hh - sub < nheads; hh += 4 * HPW) {
-    const bool active = hh < nheads;
-    const bool isq = hh < p.hq;
-    const T* src = isq ? static_cast<const T*>(p.q) + t * p.q_stride + static_cast<int64_t>(hh) * HD
-                       : static_cast<const T*>(p.k) + t * p.k_stride + static_cast<int64_t>(hh - p.hq) * HD;
-    float xa[PE] = {0.f, 0.f, 0.f, 0.f}, xb[PE] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
-      Vec4<T>::load(src + l * PE, xa);
-      Vec4<T>::load(src + HD / 2 + l * PE, xb);
+  int done = 0;  // tokens finished (their stages consumed)
+  for (int i = 0; i < n_mine; ++i) {
+    const int64_t t = t0 + i * dt;
+    const int pos = pos_next;
+    const int64_t slot = slot_next;
+    if (i + 1 < n_mine) {  // the next token's metadata, one token ahead
+      pos_next = p.positions[t + dt];
+      slot_next = p.slots[t + dt];
     }
-    float ss = 0.f;
+    const bool slot_ok = slot >= 0 && slot < p.num_slots;
+    if (!slot_ok && slot != -1 && threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_SLOT);
+    // cos / sin of the token's HD/2 pair indices, one thread per pair: the
+    // angle pos * theta^(-2i/HD) formed and reduced modulo 2*pi in two-float
+    // arithmetic, then evaluated by the special-function unit
+    if (threadIdx.x < HD / 2) {
+      const float r = reduce_angle(pos, p.inv_freq_hi[threadIdx.x], p.inv_freq_lo[threadIdx.x]);
+      float sv, cv;
+      __sincosf(r, &sv, &cv);
+      cs_s[threadIdx.x] = cv;
+      sn_s[threadIdx.x] = sv;
+    }
+    const bool ok = mbar_wait_bounded(&full[i & 1], (i >> 1) & 1, &abort_flag, p.err);
+    cta_sync();  // cos / sin written, every thread past its wait
+    if (!__syncthreads_and(ok)) break;
+    float cs[PE], sn[PE], nsn[PE];
 #pragma unroll
-    for (int e = 0; e < PE; ++e) ss += xa[e] * xa[e] + xb[e] * xb[e];
-#pragma unroll
-    for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    if (!active) continue;
-    const float r = 1.0f / sqrtf(ss / HD + p.eps);
-    T* dst = isq ? static_cast<T*>(p.q_out) + (t * p.hq + hh) * HD
-                 : static_cast<T*>(p.k_cache) + (slot * p.hkv + (hh - p.hq)) * HD;
-    const bool store = isq || slot_ok;
-    if constexpr (sizeof(T) == 2) {
-      // pairs of elements in packed fp32 arithmetic; each bf16 rounding is one
-      // two-lane conversion, the last one the store's packing:
-      // y_a = n_a cos - n_b sin, y_b = n_b cos + n_a sin
-      uint32_t wa[PE / 2], wb[PE / 2];
-      const float2 r2 = make_float2(r, r);
-#pragma unroll
-      for (int e2 = 0; e2 < PE / 2; ++e2) {
-        const int e = 2 * e2;
-        const float2 gwa = isq ? make_float2(wq_a[e], wq_a[e + 1]) : make_float2(wk_a[e], wk_a[e + 1]);
-        const float2 gwb = isq ? make_float2(wq_b[e], wq_b[e + 1]) : make_float2(wk_b[e], wk_b[e + 1]);
-        float2 ta = fmul2(make_float2(xa[e], xa[e + 1]), r2);
-        float2 tb = fmul2(make_float2(xb[e], xb[e + 1]), r2);
-        ta = fmul2(bf16x2_to_float2(pack_bf16x2(ta.x, ta.y)), gwa);
-        tb = fmul2(bf16x2_to_float2(pack_bf16x2(tb.x, tb.y)), gwb);
-        const float2 na = bf16x2_to_float2(pack_bf16x2(ta.x, ta.y));
-        const float2 nb = bf16x2_to_float2(pack_bf16x2(tb.x, tb.y));
-        const float2 c2 = make_float2(cs[e], cs[e + 1]);
-        const float2 ya = ffma2(nb, make_float2(nsn[e], nsn[e + 1]), fmul2(na, c2));
-        const float2 yb = ffma2(nb, c2, fmul2(na, make_float2(sn[e], sn[e + 1])));
-        wa[e2] = pack_bf16x2(ya.x, ya.y);
-        wb[e2] = pack_bf16x2(yb.x, yb.y);
+    for (int e = 0; e < PE; ++e) {
+      cs[e] = cs_s[l * PE + e];
+      sn[e] = sn_s[l * PE + e];
+      nsn[e] = -sn[e];
+    }
+    const unsigned char* st = stages + (i & 1) * stage_bytes;
+    const int nheads = p.hq + p.hkv;
+    for (int hh = warp * HPW + sub; hh - sub < nheads; hh += (kNrThreads / 32) * HPW) {
+      const bool active = hh < nheads;
+      const bool isq = hh < p.hq;
+      const T* src = reinterpret_cast<const T*>(st) + static_cast<int64_t>(active ? hh : 0) * HD;
+      float xa[PE] = {0.f, 0.f, 0.f, 0.f}, xb[PE] = {0.f, 0.f, 0.f, 0.f};
+      if (active) {
+        Vec4<T>::load(src + l * PE, xa);
+        Vec4<T>::load(src + HD / 2 + l * PE, xb);
       }
-      if (store) {
-        *reinterpret_cast<uint2*>(dst + l * PE) = make_uint2(wa[0], wa[1]);
-        *reinterpret_cast<uint2*>(dst + HD / 2 + l * PE) = make_uint2(wb[0], wb[1]);
-      }
-    } else {
-      float ya[PE], yb[PE];
+      float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < PE; ++e) {
-        const float na = round_to<T>(round_to<T>(xa[e] * r) * (isq ? wq_a[e] : wk_a[e]));
-        const float nb = round_to<T>(round_to<T>(xb[e] * r) * (isq ? wq_b[e] : wk_b[e]));
-        ya[e] = round_to<T>(na * cs[e] - nb * sn[e]);
-        yb[e] = round_to<T>(nb * cs[e] + na * sn[e]);
-      }
-      if (store) {
-        Vec4<T>::store(dst + l * PE, ya);
-        Vec4<T>::store(dst + HD / 2 + l * PE, yb);
+      for (int e = 0; e < PE; ++e) ss += xa[e] * xa[e] + xb[e] * xb[e];
+#pragma unroll
+      for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      if (!active) continue;
+      const float r = 1.0f / sqrtf(ss / HD + p.eps);
+      T* dst = isq ? static_cast<T*>(p.q_out) + (t * p.hq + hh) * HD
+                   : static_cast<T*>(p.k_cache) + (slot * p.hkv + (hh - p.hq)) * HD;
+      const bool store = isq || slot_ok;
+      if constexpr (sizeof(T) == 2) {
+        // y_a = n_a cos - n_b sin, y_b = n_b cos + n_a sin on fp32 pairs
+        uint32_t wa[PE / 2], wb[PE / 2];
+        const float2 r2 = make_float2(r, r);
+#pragma unroll
+        for (int e2 = 0; e2 < PE / 2; ++e2) {
+          const int e = 2 * e2;
+          const float2 gwa = isq ? make_float2(wq_a[e], wq_a[e + 1]) : make_float2(wk_a[e], wk_a[e + 1]);
+          const float2 gwb = isq ? make_float2(wq_b[e], wq_b[e + 1]) : make_float2(wk_b[e], wk_b[e + 1]);
+          float2 ta = fmul2(make_float2(xa[e], xa[e + 1]), r2);
+          float2 tb = fmul2(make_float2(xb[e], xb[e + 1]), r2);
+          ta = fmul2(bf16x2_to_float2(pack_bf16x2(ta.x, ta.y)), gwa);
+          tb = fmul2(bf16x2_to_float2(pack_bf16x2(tb.x, tb.y)), gwb);
+          const float2 na = bf16x2_to_float2(pack_bf16x2(ta.x, ta.y));
+          const float2 nb = bf16x2_to_float2(pack_bf16x2(tb.x, tb.y));
+          const float2 c2 = make_float2(cs[e], cs[e + 1]);
+          const float2 ya = ffma2(nb, make_float2(nsn[e], nsn[e + 1]), fmul2(na, c2));
+          const float2 yb = ffma2(nb, c2, fmul2(na, make_float2(sn[e], sn[e + 1])));
+          wa[e2] = pack_bf16x2(ya.x, ya.y);
+          wb[e2] = pack_bf16x2(yb.x, yb.y);
+        }
+        if (store) {
+          *reinterpret_cast<uint2*>(dst + l * PE) = make_uint2(wa[0], wa[1]);
+          *reinterpret_cast<uint2*>(dst + HD / 2 + l * PE) = make_uint2(wb[0], wb[1]);
+        }
+      } else {
+        float ya[PE], yb[PE];
+#pragma unroll
+        for (int e = 0; e < PE; ++e) {
+          const float na = round_to<T>(round_to<T>(xa[e] * r) * (isq ? wq_a[e] : wk_a[e]));
+          const float nb = round_to<T>(round_to<T>(xb[e] * r) * (isq ? wq_b[e] : wk_b[e]));
+          ya[e] = round_to<T>(na * cs[e] - nb * sn[e]);
+          yb[e] = round_to<T>(nb * cs[e] + na * sn[e]);
+        }
+        if (store) {
+          Vec4<T>::store(dst + l * PE, ya);
+          Vec4<T>::store(dst + HD / 2 + l * PE, yb);
+        }
       }
     }
+    if (slot_ok) {  // the v row, unchanged, into its slot
+      const unsigned char* vsrc = st + row_q + row_kv;
+      char* vdst = static_cast<char*>(p.v_cache) + slot * row_kv;
+      for (int ch = threadIdx.x; ch < row_kv / 16; ch += kNrThreads)
+        stg16(vdst + ch * 16, *reinterpret_cast<const uint4*>(vsrc + ch * 16));
+    }
+    cta_sync();  // every thread is done with the stage and with cos / sin
+    if (threadIdx.x == 0 && i + 2 < n_mine) issue(i + 2);
+    done = i + 1;
   }
-  if (slot_ok) {
-    const int row_bytes = p.hkv * HD * E;
-    const char* vsrc = static_cast<const char*>(p.v) + t * p.v_stride * E;
-    char* vdst = static_cast<char*>(p.v_cache) + slot * row_bytes;
-    for (int ch = threadIdx.x; ch < row_bytes / 16; ch += blockDim.x)
-      stg16(vdst + ch * 16, ldg16(vsrc + ch * 16));
+  if (threadIdx.x == 0) {
+    // after an abort, copies issued for tokens not reached may still land:
+    // wait for them (time only) before the CTA exits
+    for (int i = done; i < n_mine && i < done + 2; ++i) {
+      const uint64_t tw = global_timer_ns();
+      while (!mbar_try_wait(&full[i & 1], (i >> 1) & 1) && global_timer_ns() - tw < kWaitLimitNs) {
+      }
+    }
   }
 }
 
@@ -249,14 +330,27 @@ cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t s) {
 
 cudaError_t launch_norm_rope_kv_write(int dtype, int head_dim, const NormRopeParams& p, cudaStream_t s) {
   if (p.n_tokens == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>(p.n_tokens);
-  if (dtype == PA_BF16) {
-    if (head_dim == 128) norm_rope_kv_write_kernel<__nv_bfloat16, 128><<<grid, 128, 0, s>>>(p);
-    else norm_rope_kv_write_kernel<__nv_bfloat16, 64><<<grid, 128, 0, s>>>(p);
-  } else {
-    if (head_dim == 128) norm_rope_kv_write_kernel<float, 128><<<grid, 128, 0, s>>>(p);
-    else norm_rope_kv_write_kernel<float, 64><<<grid, 128, 0, s>>>(p);
+  DeviceInfo di;
+  cudaError_t e = current_device_info(&di);
+  if (e != cudaSuccess) return e;
+  const int es = dtype == PA_BF16 ? 2 : 4;
+  const size_t smem = 2 * static_cast<size_t>(nr_stage_bytes(p.hq, p.hkv, head_dim, es)) + 2 * sizeof(uint64_t) +
+                      head_dim * sizeof(float);
+  if (smem > static_cast<size_t>(di.max_smem_optin)) return cudaErrorInvalidValue;
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>(p.n_tokens, static_cast<int64_t>(di.sm_count) * kNrCtasPerSm));
+  const void* fn = dtype == PA_BF16
+                       ? (head_dim == 128 ? reinterpret_cast<const void*>(norm_rope_kv_write_kernel<__nv_bfloat16, 128>)
+                                          : reinterpret_cast<const void*>(norm_rope_kv_write_kernel<__nv_bfloat16, 64>))
+                       : (head_dim == 128 ? reinterpret_cast<const void*>(norm_rope_kv_write_kernel<float, 128>)
+                                          : reinterpret_cast<const void*>(norm_rope_kv_write_kernel<float, 64>));
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
   }
+  void* args[] = {const_cast<NormRopeParams*>(&p)};
+  e = cudaLaunchKernel(fn, dim3(grid), dim3(kNrThreads), args, smem, s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

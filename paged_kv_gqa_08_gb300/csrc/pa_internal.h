@@ -84,7 +84,9 @@ struct NormRopeParams {
   unsigned int* err;
   float eps;
   int32_t hq, hkv;
-  double inv_freq[64];  // theta^(-2i/head_dim), computed on the host in double
+  // theta^(-2i/head_dim), computed on the host in double and passed as a
+  // float plus the float nearest to the remainder
+  float inv_freq_hi[64], inv_freq_lo[64];
 };
 cudaError_t launch_norm_rope_kv_write(int dtype, int head_dim, const NormRopeParams& p, cudaStream_t s);
 
