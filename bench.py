@@ -568,9 +568,13 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------
 def run_case(spec: str):
     """Profiling helper: set up the first B requests of a workload and run three
-    steps through the C ABI (no timing), e.g. --case decode:qwen3_8b_decode:16."""
+    steps through the C ABI (no timing), e.g. --case decode:qwen3_8b_decode:16;
+    kind "fused" runs the decode step as pa_decode_kv_write."""
     kind, name, nreq = spec.split(":")
     nreq = int(nreq)
+    fused = kind == "fused"
+    if fused:
+        kind = "decode"
     c = synth.CONFIGS[name]
     if nreq == c["B"]:
         wl = synth.make_workload(name)
@@ -581,7 +585,7 @@ def run_case(spec: str):
         wl = synth.make_workload(name, B=nreq)
     pa_build.build()
     load_library()
-    d = Device(wl, "cuda:0")
+    d = Device(wl, "cuda:0", fused=fused)
     for _ in range(3):
         d.write_part()
         d.attn_part()
