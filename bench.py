@@ -3,8 +3,9 @@
 
 A step is one pass of the attention hot path over one batch:
   decode (headline, the Qwen3-0.6B-shaped batch: 256 requests, 16 q / 8 kv
-  heads, head_dim 128, page size 16, contexts 128..2048): slot mapping,
-  KV write of the 256 new tokens, split-KV decode attention + merge;
+  heads, head_dim 128, page size 16, contexts 128..2048): split-KV decode
+  attention with the slot mapping and KV write of the 256 new tokens folded
+  in (pa_decode_kv_write) + merge;
   prefill (secondary): slot mapping, q/k RMSNorm + RoPE + KV write, chunked
   prefill attention over the paged prefix.
 value = algorithmic HBM bytes of the decode step / step time (GB/s), summed
