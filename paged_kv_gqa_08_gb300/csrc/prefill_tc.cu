@@ -1163,6 +1163,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 2048;   // unit lengths >= 2047 tiles share the last bucket
 constexpr int kPlanSmemPairs = 2048; // pairs kept in shared memory (the rest are re-read from the workspace)
 constexpr int kPlanCandidates = 32;  // one per warp
+constexpr int kScoreBuckets = 64;    // cost buckets per candidate when scoring it
 constexpr int kSplitWaves = 4;
 constexpr int kMaxSlots = 65535;     // slot counts are scanned in 16 bits
 
@@ -1208,6 +1209,21 @@ PA_DEVINL T block_scan_excl(T v, T* sh, T* total) {
 
 PA_DEVINL int parts_of(int nt, int tau) { return (nt + tau - 1) / tau; }
 
+// floor(a / b) for 0 <= a < 2^24 and b >= 1, given inv_b ~ 1 / b: the float
+// quotient is within one of the true one and is corrected.
+PA_DEVINL int div_near(int a, int b, float inv_b) {
+  int d = __float2int_rz(static_cast<float>(a) * inv_b);
+  if (d * b > a) --d;
+  else if ((d + 1) * b <= a) ++d;
+  return d;
+}
+
+// Dynamic shared memory of the planner: per candidate, item counts and cost
+// sums of its cost buckets and a difference array over the SMs.
+inline size_t plan_dyn_bytes(int n_sm) {
+  return static_cast<size_t>(2 * kPlanCandidates * kScoreBuckets + kPlanCandidates * (n_sm + 1)) * sizeof(int);
+}
+
 // Estimated time of a unit of `len` key tiles in steps of the attention
 // kernel (one step: a 128-key tile of a q-tile pair): a single q-tile's key
 // tiles alternate between the two softmax groups and take about 0.7 step
@@ -1221,13 +1237,15 @@ PA_DEVINL int cost_bucket(int len, int nq, int part) { return min(unit_cost(len,
 
 // A pair of nt key tiles cut into `parts` ranges: the first nt % parts ranges
 // hold one tile more than the others (lengths base + 1 and base).
+template <bool kScore>
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanParams q) {
+  extern __shared__ int plan_dyn[];  // candidate scoring: see plan_dyn_bytes
   __shared__ unsigned long long sh_scan[32];
   __shared__ int cursor[kPlanBuckets];
   __shared__ int4 sh_pairs[kPlanSmemPairs];
   __shared__ float cand_est[kPlanCandidates];
   __shared__ int cand_tau[kPlanCandidates];
-  __shared__ int sh_max_nt, sh_tau;
+  __shared__ int sh_max_nt;
   pdl_trigger();  // the attention kernel may start launching; it waits for this plan
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) sh_max_nt = 0;
@@ -1275,61 +1293,137 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
   max_nt = sh_max_nt;
   auto pair_at = [&](int i) -> int4 { return i < kPlanSmemPairs ? sh_pairs[i] : q.pairs[i]; };
 
-  // 2. the part size: one candidate per warp, from max_nt (no split) down to 2
+  // 2. the part size: one candidate per warp -- the 16 sizes from max_nt (no
+  //    split) down, each of which splits exactly the pairs longer than it, then
+  //    16 geometric steps down to 2 -- scored by the makespan of its items
+  //    dealt to the SMs longest first in snake order (SM 0, 1, .., n-1, then
+  //    n-1, .., 0, ...), which is close to the list schedule that the
+  //    persistent kernel's work counter produces from the longest-first list.
   int tau = max(max_nt, 1);
-  if (n_pairs > 0 && max_nt > 2 && q.slot_cap > 1 &&
+  if (kScore && n_pairs > 0 && max_nt > 2 && q.slot_cap > 1 &&
       static_cast<int64_t>(n_pairs) * q.Hkv <= static_cast<int64_t>(kSplitWaves) * q.n_sm) {
-    const int n_cand = min(kPlanCandidates, max_nt - 1);
-    if (warp < n_cand) {
-      const int c = warp;
-      const int t_c = max_nt <= kPlanCandidates
-                          ? max_nt - c
-                          : max(2, static_cast<int>(ceilf(max_nt * exp2f(-log2f(0.5f * max_nt) * c / (n_cand - 1)))));
-      int units = 0, slots = 0, work = 0, cmax = 0;
-      for (int i = lane; i < n_pairs; i += 32) {
-        const int4 pr = pair_at(i);
-        const int nt = pr.z, nq = pr.w;
-        const int parts = parts_of(nt, t_c);
-        const int split = parts > 1;
-        const int base = nt / parts, rem = nt - base * parts;
-        units += parts;
-        slots += split ? parts : 0;
-        work += rem * unit_cost(base + 1, nq, split) + (parts - rem) * unit_cost(base, nq, split);
-        cmax = max(cmax, unit_cost(rem ? base + 1 : base, nq, split));
+    const int c = warp;
+    int t_c;
+    if (c < kPlanCandidates / 2) {
+      t_c = max(2, max_nt - c);
+    } else {
+      const int t0 = max(2, max_nt - kPlanCandidates / 2);
+      const float f = static_cast<float>(c - kPlanCandidates / 2 + 1) / (kPlanCandidates / 2);
+      t_c = max(2, static_cast<int>(ceilf(t0 * exp2f(-log2f(0.5f * t0) * f))));
+    }
+    // this candidate's item costs, in 64 buckets of `w` cost units
+    int* cnt = plan_dyn + c * kScoreBuckets;
+    float* sum = reinterpret_cast<float*>(plan_dyn + kPlanCandidates * kScoreBuckets) + c * kScoreBuckets;
+    float* diff = reinterpret_cast<float*>(plan_dyn + 2 * kPlanCandidates * kScoreBuckets) + c * (q.n_sm + 1);
+    const int w = (unit_cost(t_c, 2, 1) + kScoreBuckets) / kScoreBuckets;
+    const float inv_t = 1.f / t_c, inv_w = 1.f / w, inv_m = 1.f / q.n_sm;
+    for (int k = lane; k < kScoreBuckets; k += 32) {
+      cnt[k] = 0;
+      sum[k] = 0.f;
+    }
+    for (int k = lane; k <= q.n_sm; k += 32) diff[k] = 0.f;
+    __syncwarp();
+    int slots = 0;
+    for (int i = lane; i < n_pairs; i += 32) {
+      const int4 pr = pair_at(i);
+      const int nt = pr.z, nq = pr.w;
+      const int parts = div_near(nt + t_c - 1, t_c, inv_t);
+      const int split = parts > 1;
+      const int base = div_near(nt, parts, 1.f / parts), rem = nt - base * parts;
+      slots += split ? parts : 0;
+      if (rem) {
+        const int cu = unit_cost(base + 1, nq, split);
+        const int bk = min(div_near(cu, w, inv_w), kScoreBuckets - 1);
+        atomicAdd(&cnt[bk], rem * q.Hkv);
+        atomicAdd(&sum[bk], static_cast<float>(rem * q.Hkv) * cu);
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        units += __shfl_xor_sync(0xffffffffu, units, o);
-        slots += __shfl_xor_sync(0xffffffffu, slots, o);
-        work += __shfl_xor_sync(0xffffffffu, work, o);
-        cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-      }
-      if (lane == 0) {
-        const float ctas = static_cast<float>(units) * q.Hkv;
-        const float waves = ceilf(ctas / q.n_sm);
-        const float mean = static_cast<float>(work) * q.Hkv / q.n_sm;
-        cand_est[c] = slots > q.slot_cap ? INFINITY : fminf(waves * cmax, mean + cmax);
-        cand_tau[c] = t_c;
+      if (parts > rem) {
+        const int cu = unit_cost(base, nq, split);
+        const int bk = min(div_near(cu, w, inv_w), kScoreBuckets - 1);
+        atomicAdd(&cnt[bk], (parts - rem) * q.Hkv);
+        atomicAdd(&sum[bk], static_cast<float>((parts - rem) * q.Hkv) * cu);
       }
     }
-    cta_sync();
-    if (warp == 0) {
-      // arg-min; ties go to the lower index (the larger part size)
-      float e = lane < n_cand ? cand_est[lane] : INFINITY;
-      int c = lane;
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float e2 = __shfl_xor_sync(0xffffffffu, e, o);
-        const int c2 = __shfl_xor_sync(0xffffffffu, c, o);
-        if (e2 < e || (e2 == e && c2 < c)) {
-          e = e2;
-          c = c2;
+    for (int o = 16; o >= 1; o >>= 1) slots += __shfl_xor_sync(0xffffffffu, slots, o);
+    __syncwarp();
+    // deal: lane k owns buckets 63 - k and 31 - k (descending cost order);
+    // the items of a bucket take the next positions of the deal, each worth
+    // the bucket's mean cost, as a difference array over the SMs plus whole
+    // rounds that reach every SM
+    const int M = q.n_sm;
+    int n_a = cnt[kScoreBuckets - 1 - lane], n_b = cnt[kScoreBuckets / 2 - 1 - lane];
+    int pos_a = n_a, pos_b = n_b;  // inclusive scans, then exclusive
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ya = __shfl_up_sync(0xffffffffu, pos_a, o), yb = __shfl_up_sync(0xffffffffu, pos_b, o);
+      if (lane >= o) {
+        pos_a += ya;
+        pos_b += yb;
+      }
+    }
+    const int total_a = __shfl_sync(0xffffffffu, pos_a, 31);
+    pos_a -= n_a;
+    pos_b += total_a - n_b;
+    float rounds = 0.f;
+    auto deal = [&](int p0, int n, float cost) {
+      const int p1 = p0 + n;
+      while (p0 < p1) {
+        const int layer = div_near(p0, M, inv_m), s0 = p0 - layer * M;
+        const int e = min(p1 - layer * M, M);  // end of this layer's part
+        if (s0 == 0 && e == M) {
+          const int full = div_near(p1 - p0, M, inv_m);  // whole rounds
+          rounds += cost * full;
+          p0 += full * M;
+          continue;
         }
+        const int lo = (layer & 1) ? M - e : s0, hi = (layer & 1) ? M - s0 : e;
+        atomicAdd(&diff[lo], cost);
+        atomicAdd(&diff[hi], -cost);
+        p0 = layer * M + e;
       }
-      if (lane == 0) sh_tau = e < INFINITY ? cand_tau[c] : max_nt;  // candidate 0 (no split) is always finite
+    };
+    if (n_a > 0) deal(pos_a, n_a, sum[kScoreBuckets - 1 - lane] / n_a);
+    if (n_b > 0) deal(pos_b, n_b, sum[kScoreBuckets / 2 - 1 - lane] / n_b);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) rounds += __shfl_xor_sync(0xffffffffu, rounds, o);
+    __syncwarp();
+    // loads: prefix sums of the difference array, contiguous runs per lane
+    const int per = (M + 31) / 32, m0 = min(M, lane * per), m1 = min(M, m0 + per);
+    float run = 0.f, best = 0.f;
+    for (int m = m0; m < m1; ++m) run += diff[m];
+    float pre = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += y;
+    }
+    run = pre - run;  // load before this lane's first SM
+    for (int m = m0; m < m1; ++m) {
+      run += diff[m];
+      best = fmaxf(best, run);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if (lane == 0) {
+      cand_est[c] = slots > q.slot_cap ? INFINITY : best + rounds;
+      cand_tau[c] = t_c;
     }
     cta_sync();
-    tau = sh_tau;
+    // every warp takes the arg-min; ties go to the lower index (the larger
+    // part size); candidate 0 (no split) is always finite
+    float e = cand_est[lane];
+    int cc = lane;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float e2 = __shfl_xor_sync(0xffffffffu, e, o);
+      const int c2 = __shfl_xor_sync(0xffffffffu, cc, o);
+      if (e2 < e || (e2 == e && c2 < cc)) {
+        e = e2;
+        cc = c2;
+      }
+    }
+    tau = e < INFINITY ? cand_tau[cc] : max_nt;
   }
 
   // 3. histogram of unit costs, then bucket cursors in descending cost order
@@ -1604,6 +1698,11 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
       if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
       e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
+      int n_sm = 0;
+      if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(prefill_plan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(plan_dyn_bytes(n_sm)));
+      if (e != cudaSuccess) return e;
       done[dev] = true;
     }
   }
@@ -1638,7 +1737,12 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   q.pair_cap = pl.pair_cap;
   q.slot_cap = pl.run_slot_cap;
   q.split_cap = pl.run_split_cap;
-  prefill_plan_kernel<<<1, kPlanThreads, 0, s>>>(q);
+  // part sizes are scored only when the call may split (when its tokens
+  // alone make pairs that fill more than kSplitWaves waves it may not)
+  if (q.slot_cap > 1)
+    prefill_plan_kernel<true><<<1, kPlanThreads, plan_dyn_bytes(pl.n_sm), s>>>(q);
+  else
+    prefill_plan_kernel<false><<<1, kPlanThreads, 0, s>>>(q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   p.units = q.units;
