@@ -1141,24 +1141,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 // ---------------------------------------------------------------------------
 // planner: q-tile pairs -> units (split long key ranges, longest first)
 // ---------------------------------------------------------------------------
-// A CTA of the attention kernel runs one unit.  Without a plan the units are
-// the q-tile pairs themselves in grid order, so a batch whose pairs fill less
-// than a wave, or whose last wave holds its longest pairs, waits on its
-// longest pair.  The planner (one CTA, on the device, so the launch needs no
-// host copy of the lengths and can be captured in a graph) lists the pairs
-// with their key-tile counts nt, chooses a part size tau, cuts every pair
-// with nt > tau into ceil(nt / tau) near-equal key ranges, and writes the
-// units sorted by length, longest first, so that the hardware block
-// scheduler, which starts CTAs in index order as SMs free up, approximates
-// longest-processing-time-first list scheduling.
+// Without a plan each CTA of the attention kernel runs one q-tile pair in
+// grid order, so a batch whose pairs fill less than a wave, or whose last
+// wave holds its longest pairs, waits on its longest pair.  The planner (one
+// CTA, on the device, so the launch needs no host copy of the lengths and can
+// be captured in a graph) lists the pairs with their key-tile counts nt,
+// chooses a part size tau, cuts every pair with nt > tau into ceil(nt / tau)
+// near-equal key ranges, and writes the units sorted by cost, longest first.
+// The persistent attention kernel takes (unit, kv-head) items from a shared
+// counter in that order whenever a CTA frees up: longest-processing-time-
+// first list scheduling.
 //
-// tau minimises an estimate of the makespan in units of one key tile of one
-// CTA: a unit costs its length + 1 (prologue, epilogue) + 1 more when it is a
-// part (partial store, merge); with U CTAs of largest cost c_max and mean
-// load A = total cost / SMs, the estimate is min(ceil(U / SMs) * c_max,
-// A + c_max) (the waves bound and the list-scheduling bound).  Splitting is
-// considered only while the pairs fill at most four waves; beyond that the
-// ordering alone keeps the tail short.
+// tau is chosen among 32 candidates by the makespan of their items dealt to
+// the SMs longest first in snake order, in units of one key tile of a q-tile
+// pair (unit_cost).  Splitting is considered only while the pairs fill at
+// most four waves; beyond that the ordering alone keeps the tail short.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 2048;   // unit lengths >= 2047 tiles share the last bucket
 constexpr int kPlanSmemPairs = 2048; // pairs kept in shared memory (the rest are re-read from the workspace)
