@@ -134,6 +134,14 @@ PA_DEVINL float reduce_angle(int pos, float fh, float fl) {
   return r + (e1 + e2);
 }
 
+// Two bf16 products, each rounded once to bf16 (the exact product of two
+// bf16 values fits in fp32, so this equals rounding the fp32 product).
+PA_DEVINL uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 constexpr int kNrThreads = 128;
 constexpr int kNrCtasPerSm = 8;
 
@@ -192,6 +200,15 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
   Vec4<T>::load(static_cast<const T*>(p.wq) + HD / 2 + l * PE, wq_b);
   Vec4<T>::load(static_cast<const T*>(p.wk) + l * PE, wk_a);
   Vec4<T>::load(static_cast<const T*>(p.wk) + HD / 2 + l * PE, wk_b);
+  // bf16: the weights as bf16 pairs for the packed multiply
+  uint32_t wq_a2[PE / 2], wq_b2[PE / 2], wk_a2[PE / 2], wk_b2[PE / 2];
+#pragma unroll
+  for (int e2 = 0; e2 < PE / 2; ++e2) {
+    wq_a2[e2] = pack_bf16x2(wq_a[2 * e2], wq_a[2 * e2 + 1]);
+    wq_b2[e2] = pack_bf16x2(wq_b[2 * e2], wq_b[2 * e2 + 1]);
+    wk_a2[e2] = pack_bf16x2(wk_a[2 * e2], wk_a[2 * e2 + 1]);
+    wk_b2[e2] = pack_bf16x2(wk_b[2 * e2], wk_b[2 * e2 + 1]);
+  }
   int pos_next = n_mine > 0 ? p.positions[t0] : 0;
   int64_t slot_next = n_mine > 0 ? p.slots[t0] : -1;
   cta_sync();
@@ -238,13 +255,17 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
         Vec4<T>::load(src + l * PE, xa);
         Vec4<T>::load(src + HD / 2 + l * PE, xb);
       }
-      float ss = 0.f;
+      float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < PE; ++e) ss += xa[e] * xa[e] + xb[e] * xb[e];
+      for (int e = 0; e < PE; e += 2) {
+        ss2 = ffma2(make_float2(xa[e], xa[e + 1]), make_float2(xa[e], xa[e + 1]), ss2);
+        ss2 = ffma2(make_float2(xb[e], xb[e + 1]), make_float2(xb[e], xb[e + 1]), ss2);
+      }
+      float ss = ss2.x + ss2.y;
 #pragma unroll
       for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
       if (!active) continue;
-      const float r = 1.0f / sqrtf(ss / HD + p.eps);
+      const float r = rsqrtf(ss * (1.0f / HD) + p.eps);
       T* dst = isq ? static_cast<T*>(p.q_out) + (t * p.hq + hh) * HD
                    : static_cast<T*>(p.k_cache) + (slot * p.hkv + (hh - p.hq)) * HD;
       const bool store = isq || slot_ok;
@@ -255,14 +276,10 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
 #pragma unroll
         for (int e2 = 0; e2 < PE / 2; ++e2) {
           const int e = 2 * e2;
-          const float2 gwa = isq ? make_float2(wq_a[e], wq_a[e + 1]) : make_float2(wk_a[e], wk_a[e + 1]);
-          const float2 gwb = isq ? make_float2(wq_b[e], wq_b[e + 1]) : make_float2(wk_b[e], wk_b[e + 1]);
-          float2 ta = fmul2(make_float2(xa[e], xa[e + 1]), r2);
-          float2 tb = fmul2(make_float2(xb[e], xb[e + 1]), r2);
-          ta = fmul2(bf16x2_to_float2(pack_bf16x2(ta.x, ta.y)), gwa);
-          tb = fmul2(bf16x2_to_float2(pack_bf16x2(tb.x, tb.y)), gwb);
-          const float2 na = bf16x2_to_float2(pack_bf16x2(ta.x, ta.y));
-          const float2 nb = bf16x2_to_float2(pack_bf16x2(tb.x, tb.y));
+          const float2 ta = fmul2(make_float2(xa[e], xa[e + 1]), r2);
+          const float2 tb = fmul2(make_float2(xb[e], xb[e + 1]), r2);
+          const float2 na = bf16x2_to_float2(mul_bf16x2(pack_bf16x2(ta.x, ta.y), isq ? wq_a2[e2] : wk_a2[e2]));
+          const float2 nb = bf16x2_to_float2(mul_bf16x2(pack_bf16x2(tb.x, tb.y), isq ? wq_b2[e2] : wk_b2[e2]));
           const float2 c2 = make_float2(cs[e], cs[e + 1]);
           const float2 ya = ffma2(nb, make_float2(nsn[e], nsn[e + 1]), fmul2(na, c2));
           const float2 yb = ffma2(nb, c2, fmul2(na, make_float2(sn[e], sn[e + 1])));
