@@ -531,6 +531,16 @@ def cpu_baseline(wl, budget_s: float = 15.0):
                       f"to BLAS (OPENBLAS/OMP threads {BLAS_THREADS}), {el:.1f} s"}
 
 
+def headline_config(wl, world: int) -> dict:
+    """The headline workload's config, the same on both arms."""
+    return {"workload": describe(wl), "step": "slot mapping and KV write fused into split-KV decode "
+            "(pa_decode_kv_write) + LSE merge, launched as one CUDA graph",
+            "global_batch": world * wl.batch, "kv_bytes_per_step": kv_bytes(wl),
+            "algorithmic_bytes_per_step": decode_call_bytes(wl) + fused_write_bytes(wl),
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (KV cache 1.1 GB > 129 MB L2); no flush"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -553,13 +563,14 @@ def run_reference(args, rank, world):
         tot_bytes += sample_bytes(wl, reqs)
     el = time.perf_counter() - t0
     value = tot_bytes / el / 1e9
-    sample = (f"each step: {n_req} random requests of {wl.name} through the float64 oracle, {HOST_CORES} host "
+    sample = (f"each step: {n_req} of the {wl.batch} requests of {wl.name} (random) through the float64 oracle "
+              f"(slot mapping, KV write, attention), {HOST_CORES} host "
               f"cores available to BLAS (OPENBLAS/OMP threads {BLAS_THREADS})")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, synth/)",
-            "config": {"workload": describe(wl), "sample_requests_per_step": n_req},
+            "config": headline_config(wl, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": HOST_CORES, "kind": "oracle",
                              "blas_threads": BLAS_THREADS, "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -661,11 +672,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic (seeded, synth/)",
-        "config": {"workload": describe(wl), "step": "slot mapping and KV write fused into split-KV decode "
-                   "(pa_decode_kv_write) + LSE merge, launched as one CUDA graph",
-                   "global_batch": world * wl.batch, "kv_bytes_per_step": kv_bytes(wl),
-                   "algorithmic_bytes_per_step": step_bytes, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (KV cache 1.1 GB > 129 MB L2); no flush"},
+        "config": headline_config(wl, world),
         "attn_tok_per_s": tok_s,
         "hbm_frac_of_step": value / world / hbm_peak,
         "roofline": {"kernel": "pa_decode_kv_write (plan + split-KV decode with KV write + merge kernels)",
