@@ -235,8 +235,7 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
       sn_s[threadIdx.x] = sv;
     }
     const bool ok = mbar_wait_bounded(&full[i & 1], (i >> 1) & 1, &abort_flag, p.err);
-    cta_sync();  // cos / sin written, every thread past its wait
-    if (!__syncthreads_and(ok)) break;
+    if (!__syncthreads_and(ok)) break;  // cos / sin written, every thread past its wait
     float cs[PE], sn[PE], nsn[PE];
 #pragma unroll
     for (int e = 0; e < PE; ++e) {
