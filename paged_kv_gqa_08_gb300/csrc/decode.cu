@@ -305,6 +305,7 @@ PA_DEVINL void mma_consumer(const KParams& p, unsigned char* smem, uint64_t* ful
   float o[16][2];     // O row gq, columns 8j + 2tq, 8j + 2tq + 1
   float m_run = -INFINITY, l_part = 0.f;
   int b = 0;
+  uint4 nrow = make_uint4(0, 0, 0, 0);  // this head's piece of the request's new K (lanes 0-15) / V row
 
   for (int x = x0, it = 0; x < x1; ++x, ++it) {
     const int s = it % NS;
@@ -314,6 +315,10 @@ PA_DEVINL void mma_consumer(const KParams& p, unsigned char* smem, uint64_t* ful
     const int n = md.y, flags = md.z;
 
     if (flags & 1) {  // first chunk of this CTA's share of request b
+      if ((flags & 16) && p.k_new != nullptr)  // the share ends the request: its new row, early
+        nrow = *reinterpret_cast<const uint4*>(
+            (lane < 16 ? p.k_new + static_cast<int64_t>(b) * p.k_new_stride
+                       : p.v_new + static_cast<int64_t>(b) * p.v_new_stride) + h * RB + (lane & 15) * 16);
       const char* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + h * G + (row_live ? gq : 0)) * RB;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -329,18 +334,23 @@ PA_DEVINL void mma_consumer(const KParams& p, unsigned char* smem, uint64_t* ful
     unsigned char* kst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes + h * RB;
     unsigned char* vst = kst + p.chunk_bytes;
     if (md.w >= 0) {
-      // fused KV write: this head's piece of the new row (row n - 1) goes to its slot
+      // fused KV write: this head's piece of the new row (row n - 1), read by
+      // the consumer from k_new / v_new at the start of the share (not copied
+      // by the producer, so they may be in pinned host memory), goes into the
+      // stage for the products and to its slot
       const int64_t dst_off = static_cast<int64_t>(md.w) * p.row_bytes + h * RB;
-      const unsigned char* src = (lane < 16 ? kst : vst) + (n - 1) * p.row_pitch + (lane & 15) * 16;
+      *reinterpret_cast<uint4*>((lane < 16 ? kst : vst) + (n - 1) * p.row_pitch + (lane & 15) * 16) = nrow;
       char* dst = const_cast<char*>(lane < 16 ? p.k_cache : p.v_cache) + dst_off + (lane & 15) * 16;
-      stg16(dst, *reinterpret_cast<const uint4*>(src));
+      stg16(dst, nrow);
     }
     if (n < kMmaTok) {
       // a ragged chunk: the V rows past its end meet probability 0 and must be
-      // finite (they may hold another chunk's data or nothing yet); the fence
-      // orders these stores before the copies that refill the stage later
+      // finite (they may hold another chunk's data or nothing yet)
       for (int r = n; r < kMmaTok; ++r)
         if (lane < 16) *reinterpret_cast<uint4*>(vst + r * p.row_pitch + lane * 16) = make_uint4(0, 0, 0, 0);
+    }
+    if (md.w >= 0 || n < kMmaTok) {
+      // the fence orders these stores before the copies that refill the stage later
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
@@ -504,7 +514,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD,
           off = ((static_cast<long long>(page) << p.log2P) + (t0 & (p.P - 1))) * p.row_bytes;
         }
         flags = ((x == x0 || jc == 0) ? 1 : 0) | ((x == x1 - 1 || x == cb1 - 1) ? 2 : 0) |
-                ((cb0 >= x0 && cb1 <= x1) ? 4 : 0) | ((x == cb1 - 1) ? 8 : 0);
+                ((cb0 >= x0 && cb1 <= x1) ? 4 : 0) | ((x == cb1 - 1) ? 8 : 0) | ((cb1 <= x1) ? 16 : 0);
         if (p.k_new != nullptr && (flags & 8) && n >= 1)
           new_slot = static_cast<int>(off / p.row_bytes) + n - 1;  // position context_len - 1
       }
@@ -524,7 +534,9 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD,
           } else {
             meta[s] = make_int4(ub, un, uf, uslot);
             const uint32_t bytes = static_cast<uint32_t>(un) * static_cast<uint32_t>(p.row_bytes);
-            mbar_arrive_expect_tx(&full[s], 2 * bytes);
+            // tensor-core consumers read the new token's row themselves
+            const uint32_t copied = kMma && uslot >= 0 ? bytes - static_cast<uint32_t>(p.row_bytes) : bytes;
+            mbar_arrive_expect_tx(&full[s], 2 * copied);
             unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
             if constexpr (kMma) {
               // the row copies are issued by the whole warp below
@@ -555,21 +567,17 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD,
         if constexpr (kMma) {
           // one copy per token row into rows of row_pitch bytes (the pad keeps
           // the MMA consumers' fragment loads free of bank conflicts): lane r
-          // copies K row r, lane 16 + r V row r; the new token's row comes
-          // from k_new / v_new
+          // copies K row r, lane 16 + r V row r; the new token's row is read
+          // by the consumers from k_new / v_new
           __syncwarp();
           const int s = (xg - x0 + u) % kStages;
           unsigned char* dst = smem + static_cast<size_t>(s) * 2 * p.chunk_bytes;
           const int r = lane & 15;
           const bool isv = lane >= 16;
-          if (r < un) {
+          if (r < un && !(uslot >= 0 && r == un - 1)) {
             unsigned char* d = dst + (isv ? p.chunk_bytes : 0) + r * p.row_pitch;
-            if (uslot >= 0 && r == un - 1) {
-              bulk_g2s(d, isv ? p.v_new + ub * p.v_new_stride : p.k_new + ub * p.k_new_stride, p.row_bytes, &full[s]);
-            } else {
-              const char* src = (isv ? p.v_cache : p.k_cache) + uoff + static_cast<int64_t>(r) * p.row_bytes;
-              bulk_g2s_hint(d, src, p.row_bytes, &full[s], pol);
-            }
+            const char* src = (isv ? p.v_cache : p.k_cache) + uoff + static_cast<int64_t>(r) * p.row_bytes;
+            bulk_g2s_hint(d, src, p.row_bytes, &full[s], pol);
           }
         }
       }

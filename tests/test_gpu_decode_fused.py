@@ -88,19 +88,19 @@ def test_fused_decode_reports_skipped_requests():
 
 
 @pytest.mark.parametrize("name", ["qwen3_0p6b_decode", "long_context_decode"])
-def test_fused_decode_with_q_and_out_in_pinned_host_memory(name):
+def test_fused_decode_with_inputs_and_out_in_pinned_host_memory(name):
     # Pinned host memory is mapped into the device's address space: the
-    # kernels read q and write the output (decode kernel and merge) there
-    # directly, as the end-to-end benchmark does.
+    # kernels read q and the new K / V rows and write the output (decode
+    # kernel and merge) there directly, as the end-to-end benchmark does.
     wl = synth.make_workload(name)
     run = GpuCase(wl)
     t = run.t
     row = wl.num_kv_heads * wl.head_dim
-    q_host = t["q"].cpu().pin_memory()
+    q_host, k_host, v_host = (t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new"))
     out_host = torch.full(tuple(run.bufs.out.shape), float("nan"), dtype=run.bufs.out.dtype).pin_memory()
     slots = torch.full((wl.batch,), -7, dtype=torch.int64, device="cuda")
     pa_read_device_errors(reset=True)
-    pa_decode_kv_write(run.desc, q_host, t["k_new"], row, t["v_new"], row, wl.batch, run.k_cache, run.v_cache,
+    pa_decode_kv_write(run.desc, q_host, k_host, row, v_host, row, wl.batch, run.k_cache, run.v_cache,
                        t["block_tables"], wl.max_pages_per_seq, t["context_lens"], wl.max_context_len, wl.scale, 0,
                        slots, out_host, run.bufs.workspace)
     torch.cuda.synchronize()
