@@ -6,8 +6,8 @@
  * pointer" means an address the kernels can access: device memory, or pinned
  * host memory mapped into the device's address space (cudaHostAlloc /
  * cudaHostRegister), which the kernels then read or write over the host link
- * -- pa_decode and pa_decode_kv_write accept q and out there, and for bf16
- * with head_dim 128 pa_decode_kv_write also k_new / v_new (tested); the
+ * -- for bf16 with head_dim 128, pa_decode and pa_decode_kv_write accept q
+ * and out there, and pa_decode_kv_write also k_new / v_new (tested); the
  * caches, metadata and workspaces must be device memory.  The caller
  * owns every buffer (inputs, caches, outputs, workspace); the library
  * allocates no device memory.  Every call validates its arguments on the host
