@@ -106,3 +106,23 @@ def test_fused_decode_with_inputs_and_out_in_pinned_host_memory(name):
     torch.cuda.synchronize()
     _check_all(run, wl, out_host, slots)
     assert pa_read_device_errors(reset=True) == 0
+
+
+def test_unfused_decode_with_q_and_out_in_pinned_host_memory():
+    # pa_decode on the tensor-core path: q read and the output written (decode
+    # kernel and merge) in pinned host memory, after the KV write on the device
+    from paged_kv_gqa_08_gb300 import pa_decode
+    wl = synth.make_workload("qwen3_8b_decode")
+    run = GpuCase(wl)
+    run.step()                                   # writes the new rows (and decodes) on the device
+    torch.cuda.synchronize()
+    q_host = run.t["q"].cpu().pin_memory()
+    out_host = torch.full(tuple(run.bufs.out.shape), float("nan"), dtype=run.bufs.out.dtype).pin_memory()
+    pa_read_device_errors(reset=True)
+    pa_decode(run.desc, q_host, wl.batch, run.k_cache, run.v_cache, run.t["block_tables"], wl.max_pages_per_seq,
+              run.t["context_lens"], wl.max_context_len, wl.scale, 0, out_host, run.bufs.workspace)
+    torch.cuda.synchronize()
+    ref = oracle.reference_step(wl)
+    ok, err, bound = oracle.within_tolerance(as_f64(out_host[: wl.batch]), ref["o"], wl.dtype)
+    assert ok, (err, bound)
+    assert pa_read_device_errors(reset=True) == 0
