@@ -246,18 +246,21 @@ class Device:
     def write_part(self):
         """Slot mapping + (norm/rope +) KV write: everything before attention."""
         wl, t, b = self.wl, self.t, self.bufs
-        from paged_kv_gqa_08_gb300 import pa_kv_write, pa_qk_norm_rope_kv_write, pa_slot_mapping
+        from paged_kv_gqa_08_gb300 import pa_kv_write, pa_prefill_qk_norm_rope_kv_write, pa_slot_mapping
         n = wl.num_new_tokens
         if self.fused:
             return
-        pa_slot_mapping(self.desc, wl.batch, t["cu_seqlens_q"], t["context_lens"], t["block_tables"],
-                        wl.max_pages_per_seq, n, b.positions, b.slots)
         if wl.q_norm_w is not None:
+            # slot mapping, q/k norm and rotary, KV write: one kernel
             q = t["q"]
-            pa_qk_norm_rope_kv_write(self.desc, q, q.stride(0), t["k_new"], t["k_new"].stride(0), t["v_new"],
-                                     t["v_new"].stride(0), n, b.positions, t["q_norm_w"], t["k_norm_w"], wl.eps,
-                                     wl.rope_theta, b.slots, b.q_out, self.k_cache, self.v_cache)
+            pa_prefill_qk_norm_rope_kv_write(self.desc, q, q.stride(0), t["k_new"], t["k_new"].stride(0), t["v_new"],
+                                             t["v_new"].stride(0), n, t["cu_seqlens_q"], wl.batch, t["context_lens"],
+                                             t["block_tables"], wl.max_pages_per_seq, t["q_norm_w"], t["k_norm_w"],
+                                             wl.eps, wl.rope_theta, b.q_out, self.k_cache, self.v_cache,
+                                             b.positions, b.slots)
         else:
+            pa_slot_mapping(self.desc, wl.batch, t["cu_seqlens_q"], t["context_lens"], t["block_tables"],
+                            wl.max_pages_per_seq, n, b.positions, b.slots)
             pa_kv_write(self.desc, t["k_new"], t["k_new"].stride(0), t["v_new"], t["v_new"].stride(0), n, b.slots,
                         self.k_cache, self.v_cache)
 

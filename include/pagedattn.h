@@ -160,6 +160,33 @@ PA_API pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void*
                                    void* v_cache, pa_stream_t stream);
 
 /*
+ * pa_prefill_qk_norm_rope_kv_write -- pa_slot_mapping and
+ * pa_qk_norm_rope_kv_write of a varlen prefill batch in one kernel: each new
+ * token's position and cache slot are derived from the batch metadata as
+ * pa_slot_mapping derives them (nano-vLLM learning note, prepare_prefill
+ * listing), then its q and k are normed and rotated and (k, v) written.
+ *
+ *   q, k, v, q_norm_w, k_norm_w, eps, rope_theta, q_out, k_cache, v_cache
+ *                    as pa_qk_norm_rope_kv_write.
+ *   cu_seqlens_q, batch, context_lens, block_tables, max_pages_per_seq
+ *                    as pa_slot_mapping (padding rows: position 0, slot -1).
+ *   positions_out    optional int32 [num_tokens]: the positions (NULL: not written).
+ *   slot_mapping_out optional int64 [num_tokens]: the slots (NULL: not written).
+ * The cache, q_out and the optional outputs are those of pa_slot_mapping
+ * followed by pa_qk_norm_rope_kv_write; the same metadata problems raise the
+ * same device flags.
+ */
+PA_API pa_status pa_prefill_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride,
+                                                  const void* k, int64_t k_row_stride, const void* v,
+                                                  int64_t v_row_stride, int64_t num_tokens,
+                                                  const int32_t* cu_seqlens_q, int32_t batch,
+                                                  const int32_t* context_lens, const int32_t* block_tables,
+                                                  int32_t max_pages_per_seq, const void* q_norm_w,
+                                                  const void* k_norm_w, float eps, float rope_theta, void* q_out,
+                                                  void* k_cache, void* v_cache, int32_t* positions_out,
+                                                  int64_t* slot_mapping_out, pa_stream_t stream);
+
+/*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
  * these host-side sizes on the CURRENT device (the split plan depends on its SM
  * count).  max_ctas: 0 for the library's choice, else an upper bound on the

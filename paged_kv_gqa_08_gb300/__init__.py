@@ -77,6 +77,8 @@ _SIGS = {
     "pa_kv_write": (_I32, [_DESC, _VP, _I64, _VP, _I64, _I64, _VP, _VP, _VP, _VP]),
     "pa_qk_norm_rope_kv_write": (_I32, [_DESC, _VP, _I64, _VP, _I64, _VP, _I64, _I64, _VP, _VP, _VP, _F32, _F32,
                                         _VP, _VP, _VP, _VP, _VP]),
+    "pa_prefill_qk_norm_rope_kv_write": (_I32, [_DESC, _VP, _I64, _VP, _I64, _VP, _I64, _I64, _VP, _I32, _VP, _VP,
+                                                _I32, _VP, _VP, _F32, _F32, _VP, _VP, _VP, _VP, _VP, _VP]),
     "pa_decode_workspace_size": (ctypes.c_size_t, [_DESC, _I32, _I32, _I32]),
     "pa_decode_plan_info": (_I32, [_DESC, _I32, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "pa_decode": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP, ctypes.c_size_t,
@@ -173,6 +175,18 @@ def pa_qk_norm_rope_kv_write(desc, q, q_row_stride, k, k_row_stride, v, v_row_st
         ctypes.byref(desc), _ptr(q), q_row_stride, _ptr(k), k_row_stride, _ptr(v), v_row_stride, num_tokens,
         _ptr(positions), _ptr(q_norm_w), _ptr(k_norm_w), eps, rope_theta, _ptr(slot_mapping), _ptr(q_out),
         _ptr(k_cache), _ptr(v_cache), _stream(stream)))
+
+
+def pa_prefill_qk_norm_rope_kv_write(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens,
+                                     cu_seqlens_q, batch, context_lens, block_tables, max_pages_per_seq, q_norm_w,
+                                     k_norm_w, eps, rope_theta, q_out, k_cache, v_cache, positions_out=None,
+                                     slot_mapping_out=None, stream=None):
+    lib = load_library()
+    _check("pa_prefill_qk_norm_rope_kv_write", lib.pa_prefill_qk_norm_rope_kv_write(
+        ctypes.byref(desc), _ptr(q), q_row_stride, _ptr(k), k_row_stride, _ptr(v), v_row_stride, num_tokens,
+        _ptr(cu_seqlens_q), batch, _ptr(context_lens), _ptr(block_tables), max_pages_per_seq, _ptr(q_norm_w),
+        _ptr(k_norm_w), eps, rope_theta, _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(positions_out),
+        _ptr(slot_mapping_out), _stream(stream)))
 
 
 def pa_decode_workspace_size(desc, batch, max_context_len, max_ctas=0) -> int:

@@ -181,18 +181,18 @@ pa_status pa_kv_write(const pa_cache_desc* desc, const void* k, int64_t k_row_st
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
-                                   int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
-                                   const int32_t* positions, const void* q_norm_w, const void* k_norm_w, float eps,
-                                   float rope_theta, const int64_t* slot_mapping, void* q_out, void* k_cache,
-                                   void* v_cache, pa_stream_t stream) {
+namespace pa {
+namespace {
+// The checks and parameters both norm / rotary entry points share; the
+// position / slot source is filled in by the caller.
+pa_status norm_rope_params(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
+                           int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
+                           const void* q_norm_w, const void* k_norm_w, float eps, float rope_theta, void* q_out,
+                           void* k_cache, void* v_cache, NormRopeParams* out) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
-  if (num_tokens < 0) return PA_ERR_SHAPE;
-  if (num_tokens == 0) return PA_OK;
-  if (num_tokens > 0x7fffffff) return PA_ERR_SHAPE;
-  if (!q || !k || !v || !positions || !q_norm_w || !k_norm_w || !slot_mapping || !q_out || !k_cache || !v_cache)
-    return PA_ERR_NULL;
+  if (num_tokens < 0 || num_tokens > 0x7fffffff) return PA_ERR_SHAPE;
+  if (!q || !k || !v || !q_norm_w || !k_norm_w || !q_out || !k_cache || !v_cache) return PA_ERR_NULL;
   if (!(eps >= 0.f) || !isfinite(eps) || !(rope_theta > 1.f) || !isfinite(rope_theta)) return PA_ERR_SHAPE;
   const int64_t re = row_elems(desc);
   const int64_t qe = static_cast<int64_t>(desc->num_q_heads) * desc->head_dim;
@@ -203,9 +203,8 @@ pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int
       !aligned16(v_cache) || !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return PA_ERR_ALIGN;
   if (q_out == q && q_row_stride != qe) return PA_ERR_SHAPE;
-  unsigned int* err = nullptr;
-  if ((st = prepare(&err)) != PA_OK) return st;
-  NormRopeParams p{};
+  NormRopeParams& p = *out;
+  p = NormRopeParams{};
   p.q = q;
   p.k = k;
   p.v = v;
@@ -213,15 +212,12 @@ pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int
   p.k_stride = k_row_stride;
   p.v_stride = v_row_stride;
   p.n_tokens = num_tokens;
-  p.positions = positions;
   p.wq = q_norm_w;
   p.wk = k_norm_w;
-  p.slots = slot_mapping;
   p.q_out = q_out;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.num_slots = desc->num_pages * desc->page_size;
-  p.err = err;
   p.eps = eps;
   p.hq = desc->num_q_heads;
   p.hkv = desc->num_kv_heads;
@@ -230,6 +226,65 @@ pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int
     p.inv_freq_hi[i] = static_cast<float>(f);
     p.inv_freq_lo[i] = static_cast<float>(f - static_cast<double>(p.inv_freq_hi[i]));
   }
+  return PA_OK;
+}
+}  // namespace
+}  // namespace pa
+
+pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
+                                   int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
+                                   const int32_t* positions, const void* q_norm_w, const void* k_norm_w, float eps,
+                                   float rope_theta, const int64_t* slot_mapping, void* q_out, void* k_cache,
+                                   void* v_cache, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  NormRopeParams p;
+  st = norm_rope_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, q_norm_w, k_norm_w, eps,
+                        rope_theta, q_out, k_cache, v_cache, &p);
+  if (st != PA_OK) return st;
+  if (!positions || !slot_mapping) return PA_ERR_NULL;
+  unsigned int* err = nullptr;
+  if ((st = prepare(&err)) != PA_OK) return st;
+  p.positions = positions;
+  p.slots = slot_mapping;
+  p.err = err;
+  cudaError_t e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_prefill_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride,
+                                           const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                                           int64_t num_tokens, const int32_t* cu_seqlens_q, int32_t batch,
+                                           const int32_t* context_lens, const int32_t* block_tables,
+                                           int32_t max_pages_per_seq, const void* q_norm_w, const void* k_norm_w,
+                                           float eps, float rope_theta, void* q_out, void* k_cache, void* v_cache,
+                                           int32_t* positions_out, int64_t* slot_mapping_out, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0 || batch < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (batch == 0 || max_pages_per_seq < 1) return PA_ERR_SHAPE;  // tokens without requests, or no pages
+  NormRopeParams p;
+  st = norm_rope_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, q_norm_w, k_norm_w, eps,
+                        rope_theta, q_out, k_cache, v_cache, &p);
+  if (st != PA_OK) return st;
+  if (!cu_seqlens_q || !context_lens || !block_tables) return PA_ERR_NULL;
+  unsigned int* err = nullptr;
+  if ((st = prepare(&err)) != PA_OK) return st;
+  p.err = err;
+  p.cu = cu_seqlens_q;
+  p.ctx = context_lens;
+  p.bt = block_tables;
+  p.batch = batch;
+  p.maxp = max_pages_per_seq;
+  p.page_size = desc->page_size;
+  p.log2P = 0;
+  while ((1 << p.log2P) < desc->page_size) ++p.log2P;
+  p.num_pages = desc->num_pages;
+  p.pos_out = positions_out;
+  p.slots_out = slot_mapping_out;
   cudaError_t e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }

@@ -142,8 +142,49 @@ PA_DEVINL uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Position and cache slot of new token t from the varlen metadata, as
+// pa_slot_mapping computes them (nano-vLLM learning note, prepare_prefill
+// listing): request b owns tokens cu[b] .. cu[b+1]-1, at positions
+// context_lens[b] - n_b + j; a padding row (length 0) and an inconsistent
+// request get position 0 and slot -1.  With `report` the flags and the
+// optional outputs are written.
+PA_DEVINL void map_token(const NormRopeParams& p, int64_t t, bool report, int& pos, int64_t& slot) {
+  int lo = 0, hi = p.batch - 1;  // the last request whose tokens start at or before t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int b = lo;
+  const int s0 = p.cu[b], s1 = p.cu[b + 1], L = p.ctx[b];
+  const int n = s1 - s0, start = L - n;
+  pos = 0;
+  slot = -1;
+  unsigned int flag = 0;
+  if (s0 < 0 || t < s0 || t >= s1 || static_cast<int64_t>(s1) > p.n_tokens) {
+    flag = PA_DEVERR_BAD_LENGTH;  // cu_seqlens_q does not cover the token
+  } else if (L == 0) {
+    // a padding row: stored nowhere
+  } else if (start < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(p.maxp) * p.page_size) {
+    flag = PA_DEVERR_BAD_LENGTH;
+  } else {
+    pos = start + static_cast<int>(t - s0);
+    const int page = p.bt[static_cast<int64_t>(b) * p.maxp + (pos >> p.log2P)];
+    if (page >= 0 && page < p.num_pages)
+      slot = static_cast<int64_t>(page) * p.page_size + (pos & (p.page_size - 1));
+    else
+      flag = PA_DEVERR_BAD_PAGE;
+  }
+  if (report) {
+    if (flag) raise_flag(p.err, flag);
+    if (p.pos_out) p.pos_out[t] = pos;
+    if (p.slots_out) p.slots_out[t] = slot;
+  }
+}
+
 constexpr int kNrThreads = 128;
 constexpr int kNrCtasPerSm = 8;
+constexpr int kNrMaxPerCta = 2048;
 
 // Shared-memory bytes of one token's stage: its q, k and v rows.
 __host__ __device__ constexpr int nr_stage_bytes(int hq, int hkv, int hd, int e) { return (hq + 2 * hkv) * hd * e; }
@@ -174,6 +215,8 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
   uint64_t* full = reinterpret_cast<uint64_t*>(nr_smem + 2 * stage_bytes);
   float* cs_s = reinterpret_cast<float*>(full + 2);   // [HD / 2]
   float* sn_s = cs_s + HD / 2;
+  // the CTA's tokens' (position, slot) when they come from the metadata
+  longlong2* meta_s = reinterpret_cast<longlong2*>(sn_s + HD / 2);
   __shared__ int abort_flag;
 
   const int64_t t0 = blockIdx.x, dt = gridDim.x;
@@ -209,19 +252,38 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
     wk_a2[e2] = pack_bf16x2(wk_a[2 * e2], wk_a[2 * e2 + 1]);
     wk_b2[e2] = pack_bf16x2(wk_b[2 * e2], wk_b[2 * e2 + 1]);
   }
-  int pos_next = n_mine > 0 ? p.positions[t0] : 0;
-  int64_t slot_next = n_mine > 0 ? p.slots[t0] : -1;
+  // a token's position and slot: from the inputs, or mapped from the varlen
+  // metadata for all of the CTA's tokens at once by warp 1 (the mapping's
+  // dependent loads overlap the first token's copies)
+  const bool mapped = p.positions == nullptr;
+  if (mapped && warp == 1)
+    for (int k = lane; k < n_mine; k += 32) {
+      int pos;
+      int64_t slot;
+      map_token(p, t0 + k * dt, true, pos, slot);
+      meta_s[k] = make_longlong2(pos, slot);
+    }
+  auto token_meta = [&](int i, int& pos, int64_t& slot) {
+    if (mapped) {
+      const longlong2 m = meta_s[i];
+      pos = static_cast<int>(m.x);
+      slot = m.y;
+    } else {
+      pos = p.positions[t0 + i * dt];
+      slot = p.slots[t0 + i * dt];
+    }
+  };
   cta_sync();
+  int pos_next = 0;
+  int64_t slot_next = -1;
+  if (n_mine > 0) token_meta(0, pos_next, slot_next);
 
   int done = 0;  // tokens finished (their stages consumed)
   for (int i = 0; i < n_mine; ++i) {
     const int64_t t = t0 + i * dt;
     const int pos = pos_next;
     const int64_t slot = slot_next;
-    if (i + 1 < n_mine) {  // the next token's metadata, one token ahead
-      pos_next = p.positions[t + dt];
-      slot_next = p.slots[t + dt];
-    }
+    if (i + 1 < n_mine) token_meta(i + 1, pos_next, slot_next);  // the next token's, one token ahead
     const bool slot_ok = slot >= 0 && slot < p.num_slots;
     if (!slot_ok && slot != -1 && threadIdx.x == 0) raise_flag(p.err, PA_DEVERR_BAD_SLOT);
     // cos / sin of the token's HD/2 pair indices, one thread per pair: the
@@ -350,11 +412,15 @@ cudaError_t launch_norm_rope_kv_write(int dtype, int head_dim, const NormRopePar
   cudaError_t e = current_device_info(&di);
   if (e != cudaSuccess) return e;
   const int es = dtype == PA_BF16 ? 2 : 4;
+  // one wave of CTAs walking the tokens, with at most kNrMaxPerCta tokens
+  // each (the mapped tokens' positions and slots are kept in shared memory)
+  const int64_t wave = static_cast<int64_t>(di.sm_count) * kNrCtasPerSm;
+  const unsigned grid = static_cast<unsigned>(
+      std::max(std::min<int64_t>(p.n_tokens, wave), (p.n_tokens + kNrMaxPerCta - 1) / kNrMaxPerCta));
+  const int64_t per_cta = (p.n_tokens + grid - 1) / grid;  // tokens of the busiest CTA
   const size_t smem = 2 * static_cast<size_t>(nr_stage_bytes(p.hq, p.hkv, head_dim, es)) + 2 * sizeof(uint64_t) +
-                      head_dim * sizeof(float);
+                      head_dim * sizeof(float) + (p.positions == nullptr ? per_cta * sizeof(longlong2) : 0);
   if (smem > static_cast<size_t>(di.max_smem_optin)) return cudaErrorInvalidValue;
-  const unsigned grid =
-      static_cast<unsigned>(std::min<int64_t>(p.n_tokens, static_cast<int64_t>(di.sm_count) * kNrCtasPerSm));
   const void* fn = dtype == PA_BF16
                        ? (head_dim == 128 ? reinterpret_cast<const void*>(norm_rope_kv_write_kernel<__nv_bfloat16, 128>)
                                           : reinterpret_cast<const void*>(norm_rope_kv_write_kernel<__nv_bfloat16, 64>))

@@ -87,6 +87,15 @@ struct NormRopeParams {
   // theta^(-2i/head_dim), computed on the host in double and passed as a
   // float plus the float nearest to the remainder
   float inv_freq_hi[64], inv_freq_lo[64];
+  // positions == nullptr: each token's position and slot come from the varlen
+  // metadata (as pa_slot_mapping computes them), optionally written out
+  const int32_t* cu;
+  const int32_t* ctx;
+  const int32_t* bt;
+  int32_t batch, maxp, page_size, log2P;
+  int64_t num_pages;
+  int32_t* pos_out;
+  int64_t* slots_out;
 };
 cudaError_t launch_norm_rope_kv_write(int dtype, int head_dim, const NormRopeParams& p, cudaStream_t s);
 

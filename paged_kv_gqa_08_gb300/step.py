@@ -13,8 +13,8 @@ from typing import Optional
 
 import torch
 
-from . import (pa_decode, pa_decode_workspace_size, pa_kv_write, pa_prefill_varlen, pa_prefill_workspace_size,
-               pa_qk_norm_rope_kv_write, pa_slot_mapping)
+from . import (pa_decode, pa_decode_workspace_size, pa_kv_write, pa_prefill_qk_norm_rope_kv_write, pa_prefill_varlen,
+               pa_prefill_workspace_size, pa_slot_mapping)
 
 
 @dataclasses.dataclass
@@ -76,16 +76,18 @@ def run_step(desc, kind: str, bufs: StepBuffers, q, k, v, cu_seqlens_q, context_
     """Run one step; returns ``bufs.out`` (the attention output of the new tokens)."""
     n = q.shape[0]
     batch = context_lens.shape[0]
-    pa_slot_mapping(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq, n, bufs.positions,
-                    bufs.slots, stream)
     q_row = desc.num_q_heads * desc.head_dim
     kv_row = desc.num_kv_heads * desc.head_dim
     if q_norm_w is not None:
-        pa_qk_norm_rope_kv_write(desc, q, q.stride(0), k, k.stride(0), v, v.stride(0), n, bufs.positions,
-                                 q_norm_w, k_norm_w, eps, rope_theta, bufs.slots, bufs.q_out, k_cache, v_cache,
-                                 stream)
+        # slot mapping, norm, rotary and KV write in one kernel
+        pa_prefill_qk_norm_rope_kv_write(desc, q, q.stride(0), k, k.stride(0), v, v.stride(0), n, cu_seqlens_q,
+                                         batch, context_lens, block_tables, max_pages_per_seq, q_norm_w, k_norm_w,
+                                         eps, rope_theta, bufs.q_out, k_cache, v_cache, bufs.positions, bufs.slots,
+                                         stream)
         qa = bufs.q_out
     else:
+        pa_slot_mapping(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq, n, bufs.positions,
+                        bufs.slots, stream)
         pa_kv_write(desc, k, k.stride(0), v, v.stride(0), n, bufs.slots, k_cache, v_cache, stream)
         qa = q
     assert q_row > 0 and kv_row > 0

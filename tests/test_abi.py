@@ -124,6 +124,24 @@ def test_norm_rope_argument_validation(lib):
     assert call(qs=16 * 128 + 8, q=FAKE, qout=FAKE) == pa.PA_ERR_SHAPE   # in place needs a dense q
 
 
+def test_prefill_norm_rope_argument_validation(lib):
+    d = _desc()
+
+    def call(n=3, batch=2, maxp=4, cu=FAKE, w=FAKE, eps=1e-6):
+        return lib.pa_prefill_qk_norm_rope_kv_write(ctypes.byref(d), FAKE, 16 * 128, FAKE, 8 * 128, FAKE, 8 * 128, n,
+                                                    cu, batch, FAKE, FAKE, maxp, w, FAKE, eps, 1e6, FAKE, FAKE,
+                                                    FAKE, None, None, None)
+
+    assert call(n=0) == pa.PA_OK
+    assert call(n=0, cu=None) == pa.PA_OK              # nothing to do: nothing checked past the sizes
+    assert call(batch=0) == pa.PA_ERR_SHAPE            # tokens without requests
+    assert call(batch=-1) == pa.PA_ERR_SHAPE
+    assert call(maxp=0) == pa.PA_ERR_SHAPE
+    assert call(cu=None) == pa.PA_ERR_NULL
+    assert call(w=None) == pa.PA_ERR_NULL
+    assert call(eps=-1.0) == pa.PA_ERR_SHAPE
+
+
 def test_prefill_argument_validation(lib):
     d = _desc()
 

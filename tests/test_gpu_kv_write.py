@@ -104,3 +104,58 @@ def test_kv_write_from_fused_qkv_rows():
     torch.cuda.synchronize()
     assert torch.equal(kc.view(128, -1)[slots], k)
     assert torch.equal(vc.view(128, -1)[slots], v)
+
+
+def _two_writes(wl, edit=None):
+    """The step's write part as pa_slot_mapping + pa_qk_norm_rope_kv_write and
+    as pa_prefill_qk_norm_rope_kv_write, on two copies of the same state."""
+    from paged_kv_gqa_08_gb300 import (pa_prefill_qk_norm_rope_kv_write, pa_qk_norm_rope_kv_write,
+                                       pa_read_device_errors, pa_slot_mapping)
+    runs, flags = [GpuCase(wl), GpuCase(wl)], []
+    n = wl.num_new_tokens
+    for k, run in enumerate(runs):
+        t = run.t
+        if edit is not None:
+            edit(t)
+        run.bufs.positions.fill_(-5)
+        run.bufs.slots.fill_(-5)
+        pa_read_device_errors(reset=True)
+        if k == 0:
+            pa_slot_mapping(run.desc, wl.batch, t["cu_seqlens_q"], t["context_lens"], t["block_tables"],
+                            wl.max_pages_per_seq, n, run.bufs.positions, run.bufs.slots)
+            pa_qk_norm_rope_kv_write(run.desc, t["q"], t["q"].stride(0), t["k_new"], t["k_new"].stride(0), t["v_new"],
+                                     t["v_new"].stride(0), n, run.bufs.positions, t["q_norm_w"], t["k_norm_w"],
+                                     wl.eps, wl.rope_theta, run.bufs.slots, run.bufs.q_out, run.k_cache, run.v_cache)
+        else:
+            pa_prefill_qk_norm_rope_kv_write(run.desc, t["q"], t["q"].stride(0), t["k_new"], t["k_new"].stride(0),
+                                             t["v_new"], t["v_new"].stride(0), n, t["cu_seqlens_q"], wl.batch,
+                                             t["context_lens"], t["block_tables"], wl.max_pages_per_seq,
+                                             t["q_norm_w"], t["k_norm_w"], wl.eps, wl.rope_theta, run.bufs.q_out,
+                                             run.k_cache, run.v_cache, run.bufs.positions, run.bufs.slots)
+        torch.cuda.synchronize()
+        flags.append(pa_read_device_errors(reset=True))
+    a, b = runs
+    assert flags[0] == flags[1]
+    assert torch.equal(a.bufs.positions[:n], b.bufs.positions[:n])
+    assert torch.equal(a.bufs.slots[:n], b.bufs.slots[:n])
+    assert torch.equal(a.bufs.q_out[:n].view(torch.int16), b.bufs.q_out[:n].view(torch.int16))
+    assert np.array_equal(_bits(storage(a.k_cache)), _bits(storage(b.k_cache)))
+    assert np.array_equal(_bits(storage(a.v_cache)), _bits(storage(b.v_cache)))
+    return flags[1]
+
+
+@pytest.mark.parametrize("name", ["qwen3_0p6b_chunked_prefill", "prefill_2k"])
+def test_prefill_write_in_one_kernel_equals_slot_mapping_then_norm_rope(name):
+    assert _two_writes(synth.make_workload(name)) == 0
+
+
+def test_prefill_write_in_one_kernel_padding_rows_and_bad_pages():
+    from paged_kv_gqa_08_gb300 import PA_DEVERR_BAD_PAGE
+    spec = dict(kind="prefill", dtype="bf16", B=5, Hq=16, Hkv=8, hd=128, P=16, chunks=[7, 40, 1, 33, 2],
+                prefixes=[0, 300, 64, 17, 5], norm=True, seed=13)
+    wl = synth.make_workload(spec)
+
+    def edit(t):
+        t["context_lens"][2] = 0                                # a padding row: position 0, slot -1, no flag
+        t["block_tables"][3, 1] = wl.num_pages + 9              # a page past the cache: slot -1, flagged
+    assert _two_writes(wl, edit) == PA_DEVERR_BAD_PAGE
