@@ -1,5 +1,6 @@
 // Slot mapping, KV scatter, and the fused per-head Q/K RMSNorm + RoPE + KV
 // scatter (sm_103a).  All three are small, latency- or HBM-bound kernels.
+#include <limits.h>
 #include <math.h>
 
 #include <algorithm>
@@ -148,15 +149,8 @@ PA_DEVINL uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 // context_lens[b] - n_b + j; a padding row (length 0) and an inconsistent
 // request get position 0 and slot -1.  With `report` the flags and the
 // optional outputs are written.
-PA_DEVINL void map_token(const NormRopeParams& p, int64_t t, bool report, int& pos, int64_t& slot) {
-  int lo = 0, hi = p.batch - 1;  // the last request whose tokens start at or before t
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.cu[mid] <= t) lo = mid;
-    else hi = mid - 1;
-  }
-  const int b = lo;
-  const int s0 = p.cu[b], s1 = p.cu[b + 1], L = p.ctx[b];
+PA_DEVINL void map_token_of(const NormRopeParams& p, int64_t t, int b, int s0, int s1, int L, bool report, int& pos,
+                             int64_t& slot) {
   const int n = s1 - s0, start = L - n;
   pos = 0;
   slot = -1;
@@ -180,6 +174,17 @@ PA_DEVINL void map_token(const NormRopeParams& p, int64_t t, bool report, int& p
     if (p.pos_out) p.pos_out[t] = pos;
     if (p.slots_out) p.slots_out[t] = slot;
   }
+}
+
+// The same for any batch: the token's request by binary search over cu.
+PA_DEVINL void map_token(const NormRopeParams& p, int64_t t, bool report, int& pos, int64_t& slot) {
+  int lo = 0, hi = p.batch - 1;  // the last request whose tokens start at or before t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  map_token_of(p, t, lo, p.cu[lo], p.cu[lo + 1], p.ctx[lo], report, pos, slot);
 }
 
 constexpr int kNrThreads = 128;
@@ -256,13 +261,37 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
   // metadata for all of the CTA's tokens at once by warp 1 (the mapping's
   // dependent loads overlap the first token's copies)
   const bool mapped = p.positions == nullptr;
-  if (mapped && warp == 1)
-    for (int k = lane; k < n_mine; k += 32) {
-      int pos;
-      int64_t slot;
-      map_token(p, t0 + k * dt, true, pos, slot);
-      meta_s[k] = make_longlong2(pos, slot);
+  if (mapped && warp == 1) {
+    if (p.batch < 32) {
+      // up to 31 requests: their cu and lengths in the lanes, one load each,
+      // so a token's request is a count of lanes, not a chain of loads
+      const int cu_l = lane <= p.batch ? p.cu[lane] : INT_MAX;
+      const int ctx_l = lane < p.batch ? p.ctx[lane] : 0;
+      for (int k0 = 0; k0 < n_mine; k0 += 32) {
+        const int k = k0 + lane;
+        const int64_t t = t0 + static_cast<int64_t>(k) * dt;
+        int b = -1;
+#pragma unroll 1
+        for (int j = 0; j < p.batch; ++j) b += __shfl_sync(0xffffffffu, cu_l, j) <= t;
+        b = max(b, 0);
+        const int s0 = __shfl_sync(0xffffffffu, cu_l, b), s1 = __shfl_sync(0xffffffffu, cu_l, b + 1);
+        const int L = __shfl_sync(0xffffffffu, ctx_l, b);
+        if (k < n_mine) {
+          int pos;
+          int64_t slot;
+          map_token_of(p, t, b, s0, s1, L, true, pos, slot);
+          meta_s[k] = make_longlong2(pos, slot);
+        }
+      }
+    } else {
+      for (int k = lane; k < n_mine; k += 32) {
+        int pos;
+        int64_t slot;
+        map_token(p, t0 + k * dt, true, pos, slot);
+        meta_s[k] = make_longlong2(pos, slot);
+      }
     }
+  }
   auto token_meta = [&](int i, int& pos, int64_t& slot) {
     if (mapped) {
       const longlong2 m = meta_s[i];
