@@ -264,6 +264,18 @@ class Device:
             pa_kv_write(self.desc, t["k_new"], t["k_new"].stride(0), t["v_new"], t["v_new"].stride(0), n, b.slots,
                         self.k_cache, self.v_cache)
 
+    def prefill_step(self):
+        """The whole prefill step in one call (pa_prefill_step: the write part,
+        then the planned attention, its planner beside the write kernel)."""
+        wl, t, b = self.wl, self.t, self.bufs
+        from paged_kv_gqa_08_gb300 import pa_prefill_step
+        q = t["q"]
+        pa_prefill_step(self.desc, q, q.stride(0), t["k_new"], t["k_new"].stride(0), t["v_new"], t["v_new"].stride(0),
+                        wl.num_new_tokens, t["cu_seqlens_q"], wl.batch, wl.max_new_len, t["context_lens"],
+                        wl.max_context_len, t["block_tables"], wl.max_pages_per_seq, t["q_norm_w"], t["k_norm_w"],
+                        wl.eps or 0.0, wl.rope_theta or 0.0, wl.scale, b.q_out, self.k_cache, self.v_cache,
+                        b.positions, b.slots, b.out, b.workspace)
+
     def attn_part(self):
         wl, t, b = self.wl, self.t, self.bufs
         q = b.q_out if wl.q_norm_w is not None else t["q"]
@@ -409,6 +421,26 @@ def time_graph_parts(d: Device, steps: int, warmup: int, flush=None, warm_s: flo
     write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     return write_ms + attn_ms, write_ms, attn_ms
+
+
+def time_graph_whole(body, steps: int, warmup: int, flush=None):
+    """`body` as one CUDA graph, L2 flushed before every replay when `flush` is
+    given; CUDA events around each replay.  Returns the mean ms."""
+    g = capture_graph(body)
+    for _ in range(warmup):
+        if flush is not None:
+            flush_l2(flush)
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for k in range(steps):
+        if flush is not None:
+            flush_l2(flush)
+        ev[k][0].record()
+        g.replay()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    return sum(e[0].elapsed_time(e[1]) for e in ev) / steps
 
 
 def step_percentiles(d: Device, n: int = 100):
@@ -716,18 +748,23 @@ def main():
     if not args.no_extra:
         extra = {"timing": "each config's KV-write part and attention call replayed as two CUDA graphs with CUDA "
                            "events around each replay, after at least 0.2 s of warm-up replays (the GPU idles "
-                           "while a config's inputs are generated on the host); prefill configs (KV fits in L2): "
-                           "L2 flushed before every step (512 MiB overwritten, then read back); decode configs "
-                           "with KV > 512 MiB: no flush"}
+                           "while a config's inputs are generated on the host); prefill configs also as the whole "
+                           "step (pa_prefill_step) in one graph, which is their ms_per_step; prefill configs (KV "
+                           "fits in L2): L2 flushed before every step (512 MiB overwritten, then read back); "
+                           "decode configs with KV > 512 MiB: no flush"}
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         for name, steps in (("qwen3_0p6b_chunked_prefill", 100), ("prefill_2k", 20)):
             w = synth.make_workload(name)
             dd = Device(w, dev)
-            step_ms, w_ms, a_ms = time_graph_parts(dd, steps, 5, flush, warm_s=0.2)
+            parts_ms, w_ms, a_ms = time_graph_parts(dd, steps, 5, flush, warm_s=0.2)
+            step_ms = time_graph_whole(dd.prefill_step, steps, 5, flush)
             fl = prefill_flops(w)
             tflops = fl / (a_ms * 1e-3) / 1e12
             rt = max(fl / (tc_peak * 1e12), prefill_call_bytes(w) / (hbm_peak * 1e9))
-            extra[name] = {"workload": describe(w), "ms_per_step": step_ms, "prefill_ms": a_ms,
+            extra[name] = {"workload": describe(w), "ms_per_step": step_ms,
+                           "step_launch": "pa_prefill_step as one CUDA graph (write kernel; planner beside it; "
+                                          "attention; merge)",
+                           "parts_ms_per_step": parts_ms, "prefill_ms": a_ms,
                            "launch": "planned (pa_prefill_varlen with workspace: plan, attention, merge)",
                            "write_ms": w_ms, "flops": fl, "tflops": tflops, "tok_per_s": w.num_new_tokens / (step_ms * 1e-3),
                            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",

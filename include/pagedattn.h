@@ -341,6 +341,39 @@ PA_API pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, con
                                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_prefill_step -- one chunked-prefill step in one call: the step's KV write
+ * (nano-vLLM learning note, Attention.forward listing: store_kvcache before
+ * the attention), then pa_prefill_varlen over the cache.
+ *
+ * With q_norm_w and k_norm_w: pa_prefill_qk_norm_rope_kv_write (q normed and
+ * rotated into q_out, positions_out and slot_mapping_out optional), then
+ * pa_prefill_varlen on q_out.  With both NULL: pa_slot_mapping into
+ * positions_out and slot_mapping_out (both required), pa_kv_write of k and v,
+ * then pa_prefill_varlen on q itself (q_row_stride must then be
+ * num_q_heads*head_dim; q_out, eps and rope_theta are unused).  One NULL
+ * weight is PA_ERR_NULL.
+ *
+ * Every argument has the meaning, layout and ownership it has in those calls;
+ * all of them are checked before anything is enqueued.  The cache, q_out,
+ * positions_out, slot_mapping_out and out are exactly those of the calls made
+ * one after another.  The difference is the launch: the attention planner
+ * (workspace given, bf16 with head_dim 128) reads only cu_seqlens_q and
+ * context_lens, which the write kernel does not write, so here it runs beside
+ * that kernel instead of after it (programmatic dependent launch; the
+ * attention kernel still starts on the cache only once the write is
+ * complete).  pa_prefill_varlen alone cannot know which kernel wrote its
+ * metadata, so its planner starts only after the previous kernel completes.
+ */
+PA_API pa_status pa_prefill_step(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
+                                 int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
+                                 const int32_t* cu_seqlens_q, int32_t batch, int32_t max_seqlen_q,
+                                 const int32_t* context_lens, int32_t max_context_len, const int32_t* block_tables,
+                                 int32_t max_pages_per_seq, const void* q_norm_w, const void* k_norm_w, float eps,
+                                 float rope_theta, float scale, void* q_out, void* k_cache, void* v_cache,
+                                 int32_t* positions_out, int64_t* slot_mapping_out, void* out, void* workspace,
+                                 size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_prefill_workspace_size -- bytes of the optional pa_prefill_varlen
  * workspace for these bounds on the current device (it holds the work list
  * and, for split ranges, fp32 partial outputs of at most 4 waves of CTAs:

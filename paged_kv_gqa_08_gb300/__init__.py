@@ -88,6 +88,8 @@ _SIGS = {
     "pa_decode_no_alloc": (_I32, [_DESC, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _I32, _VP, _VP]),
     "pa_prefill_varlen": (_I32, [_DESC, _VP, _VP, _I32, _I32, _I64, _VP, _VP, _VP, _I32, _VP, _I32, _F32, _VP, _VP,
                                  ctypes.c_size_t, _VP]),
+    "pa_prefill_step": (_I32, [_DESC, _VP, _I64, _VP, _I64, _VP, _I64, _I64, _VP, _I32, _I32, _VP, _I32, _VP, _I32,
+                               _VP, _VP, _F32, _F32, _F32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "pa_prefill_workspace_size": (ctypes.c_size_t, [_DESC, _I32, _I32, _I64, _I32]),
     "pa_validate_metadata": (_I32, [_DESC, _I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP]),
     "pa_selftest_bounded_wait": (_I32, [_I32, _VP]),
@@ -245,6 +247,21 @@ def pa_prefill_varlen(desc, q, cu_seqlens_q, batch, max_seqlen_q, num_tokens, k_
         ctypes.byref(desc), _ptr(q), _ptr(cu_seqlens_q), batch, max_seqlen_q, num_tokens, _ptr(k_cache),
         _ptr(v_cache), _ptr(block_tables), max_pages_per_seq, _ptr(context_lens), max_context_len, scale,
         _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def pa_prefill_step(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, cu_seqlens_q, batch,
+                    max_seqlen_q, context_lens, max_context_len, block_tables, max_pages_per_seq, q_norm_w, k_norm_w,
+                    eps, rope_theta, scale, q_out, k_cache, v_cache, positions_out, slot_mapping_out, out,
+                    workspace=None, workspace_bytes=None, stream=None):
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("pa_prefill_step", lib.pa_prefill_step(
+        ctypes.byref(desc), _ptr(q), q_row_stride, _ptr(k), k_row_stride, _ptr(v), v_row_stride, num_tokens,
+        _ptr(cu_seqlens_q), batch, max_seqlen_q, _ptr(context_lens), max_context_len, _ptr(block_tables),
+        max_pages_per_seq, _ptr(q_norm_w), _ptr(k_norm_w), eps, rope_theta, scale, _ptr(q_out), _ptr(k_cache),
+        _ptr(v_cache), _ptr(positions_out), _ptr(slot_mapping_out), _ptr(out), _ptr(workspace), workspace_bytes,
+        _stream(stream)))
 
 
 def pa_prefill_workspace_size(desc, batch, max_seqlen_q, num_tokens, max_context_len) -> int:

@@ -123,6 +123,57 @@ using namespace pa;
 
 extern "C" {
 
+namespace pa {
+namespace {
+// Checks of pa_slot_mapping's arguments (batch > 0) and its parameters, the
+// error word left to the caller.
+pa_status slot_map_params(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
+                          const int32_t* context_lens, const int32_t* block_tables, int32_t max_pages_per_seq,
+                          int64_t num_tokens, int32_t* positions, int64_t* slot_mapping, SlotMapParams* out) {
+  if (!cu_seqlens_q || !context_lens || !block_tables) return PA_ERR_NULL;
+  if (num_tokens > 0 && (!positions || !slot_mapping)) return PA_ERR_NULL;
+  SlotMapParams& p = *out;
+  p = SlotMapParams{};
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.context_lens = context_lens;
+  p.block_tables = block_tables;
+  p.positions = positions;
+  p.slots = slot_mapping;
+  p.num_pages = desc->num_pages;
+  p.num_tokens = num_tokens;
+  p.batch = batch;
+  p.page_size = desc->page_size;
+  p.max_pages = max_pages_per_seq;
+  return PA_OK;
+}
+
+// Checks of pa_kv_write's arguments (num_tokens > 0) and its parameters.
+pa_status kv_write_params(const pa_cache_desc* desc, const void* k, int64_t k_row_stride, const void* v,
+                          int64_t v_row_stride, int64_t num_tokens, const int64_t* slot_mapping, void* k_cache,
+                          void* v_cache, KvWriteParams* out) {
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_NULL;
+  const int64_t re = row_elems(desc);
+  if (k_row_stride < re || v_row_stride < re) return PA_ERR_SHAPE;
+  if (!stride_ok(desc, k_row_stride, re) || !stride_ok(desc, v_row_stride, re)) return PA_ERR_ALIGN;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  const int E = elem_bytes(desc->dtype);
+  KvWriteParams& p = *out;
+  p = KvWriteParams{};
+  p.k = static_cast<const char*>(k);
+  p.v = static_cast<const char*>(v);
+  p.k_stride_bytes = k_row_stride * E;
+  p.v_stride_bytes = v_row_stride * E;
+  p.n_tokens = num_tokens;
+  p.slots = slot_mapping;
+  p.k_cache = static_cast<char*>(k_cache);
+  p.v_cache = static_cast<char*>(v_cache);
+  p.num_slots = desc->num_pages * desc->page_size;
+  p.row_bytes = static_cast<int32_t>(re * E);
+  return PA_OK;
+}
+}  // namespace
+}  // namespace pa
+
 pa_status pa_slot_mapping(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
                           const int32_t* context_lens, const int32_t* block_tables, int32_t max_pages_per_seq,
                           int64_t num_tokens, int32_t* positions, int64_t* slot_mapping, pa_stream_t stream) {
@@ -130,22 +181,11 @@ pa_status pa_slot_mapping(const pa_cache_desc* desc, int32_t batch, const int32_
   if (st != PA_OK) return st;
   if (batch < 0 || num_tokens < 0 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
   if (batch == 0) return num_tokens == 0 ? PA_OK : PA_ERR_SHAPE;
-  if (!cu_seqlens_q || !context_lens || !block_tables) return PA_ERR_NULL;
-  if (num_tokens > 0 && (!positions || !slot_mapping)) return PA_ERR_NULL;
-  unsigned int* err = nullptr;
-  if ((st = prepare(&err)) != PA_OK) return st;
-  SlotMapParams p{};
-  p.cu_seqlens_q = cu_seqlens_q;
-  p.context_lens = context_lens;
-  p.block_tables = block_tables;
-  p.positions = positions;
-  p.slots = slot_mapping;
-  p.err = err;
-  p.num_pages = desc->num_pages;
-  p.num_tokens = num_tokens;
-  p.batch = batch;
-  p.page_size = desc->page_size;
-  p.max_pages = max_pages_per_seq;
+  SlotMapParams p;
+  st = slot_map_params(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq, num_tokens,
+                       positions, slot_mapping, &p);
+  if (st != PA_OK) return st;
+  if ((st = prepare(&p.err)) != PA_OK) return st;
   cudaError_t e = launch_slot_mapping(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -157,26 +197,10 @@ pa_status pa_kv_write(const pa_cache_desc* desc, const void* k, int64_t k_row_st
   if (st != PA_OK) return st;
   if (num_tokens < 0) return PA_ERR_SHAPE;
   if (num_tokens == 0) return PA_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_NULL;
-  const int64_t re = row_elems(desc);
-  if (k_row_stride < re || v_row_stride < re) return PA_ERR_SHAPE;
-  if (!stride_ok(desc, k_row_stride, re) || !stride_ok(desc, v_row_stride, re)) return PA_ERR_ALIGN;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
-  unsigned int* err = nullptr;
-  if ((st = prepare(&err)) != PA_OK) return st;
-  const int E = elem_bytes(desc->dtype);
-  KvWriteParams p{};
-  p.k = static_cast<const char*>(k);
-  p.v = static_cast<const char*>(v);
-  p.k_stride_bytes = k_row_stride * E;
-  p.v_stride_bytes = v_row_stride * E;
-  p.n_tokens = num_tokens;
-  p.slots = slot_mapping;
-  p.k_cache = static_cast<char*>(k_cache);
-  p.v_cache = static_cast<char*>(v_cache);
-  p.num_slots = desc->num_pages * desc->page_size;
-  p.row_bytes = static_cast<int32_t>(re * E);
-  p.err = err;
+  KvWriteParams p;
+  st = kv_write_params(desc, k, k_row_stride, v, v_row_stride, num_tokens, slot_mapping, k_cache, v_cache, &p);
+  if (st != PA_OK) return st;
+  if ((st = prepare(&p.err)) != PA_OK) return st;
   cudaError_t e = launch_kv_write(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -254,26 +278,22 @@ pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-pa_status pa_prefill_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride,
-                                           const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
-                                           int64_t num_tokens, const int32_t* cu_seqlens_q, int32_t batch,
-                                           const int32_t* context_lens, const int32_t* block_tables,
-                                           int32_t max_pages_per_seq, const void* q_norm_w, const void* k_norm_w,
-                                           float eps, float rope_theta, void* q_out, void* k_cache, void* v_cache,
-                                           int32_t* positions_out, int64_t* slot_mapping_out, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (num_tokens < 0 || batch < 0) return PA_ERR_SHAPE;
-  if (num_tokens == 0) return PA_OK;
+namespace pa {
+namespace {
+// Checks of pa_prefill_qk_norm_rope_kv_write's arguments (num_tokens > 0) and
+// its parameters, the error word left to the caller.
+pa_status prefill_norm_params(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
+                              int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
+                              const int32_t* cu_seqlens_q, int32_t batch, const int32_t* context_lens,
+                              const int32_t* block_tables, int32_t max_pages_per_seq, const void* q_norm_w,
+                              const void* k_norm_w, float eps, float rope_theta, void* q_out, void* k_cache,
+                              void* v_cache, int32_t* positions_out, int64_t* slot_mapping_out, NormRopeParams* out) {
   if (batch == 0 || max_pages_per_seq < 1) return PA_ERR_SHAPE;  // tokens without requests, or no pages
-  NormRopeParams p;
-  st = norm_rope_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, q_norm_w, k_norm_w, eps,
-                        rope_theta, q_out, k_cache, v_cache, &p);
+  NormRopeParams& p = *out;
+  pa_status st = norm_rope_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, q_norm_w,
+                                  k_norm_w, eps, rope_theta, q_out, k_cache, v_cache, &p);
   if (st != PA_OK) return st;
   if (!cu_seqlens_q || !context_lens || !block_tables) return PA_ERR_NULL;
-  unsigned int* err = nullptr;
-  if ((st = prepare(&err)) != PA_OK) return st;
-  p.err = err;
   p.cu = cu_seqlens_q;
   p.ctx = context_lens;
   p.bt = block_tables;
@@ -285,6 +305,28 @@ pa_status pa_prefill_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void
   p.num_pages = desc->num_pages;
   p.pos_out = positions_out;
   p.slots_out = slot_mapping_out;
+  return PA_OK;
+}
+}  // namespace
+}  // namespace pa
+
+pa_status pa_prefill_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride,
+                                           const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                                           int64_t num_tokens, const int32_t* cu_seqlens_q, int32_t batch,
+                                           const int32_t* context_lens, const int32_t* block_tables,
+                                           int32_t max_pages_per_seq, const void* q_norm_w, const void* k_norm_w,
+                                           float eps, float rope_theta, void* q_out, void* k_cache, void* v_cache,
+                                           int32_t* positions_out, int64_t* slot_mapping_out, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0 || batch < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  NormRopeParams p;
+  st = prefill_norm_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, cu_seqlens_q, batch,
+                           context_lens, block_tables, max_pages_per_seq, q_norm_w, k_norm_w, eps, rope_theta, q_out,
+                           k_cache, v_cache, positions_out, slot_mapping_out, &p);
+  if (st != PA_OK) return st;
+  if ((st = prepare(&p.err)) != PA_OK) return st;
   cudaError_t e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -397,13 +439,16 @@ pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, const voi
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
-                            int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
-                            const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
-                            int32_t max_context_len, float scale, void* out, void* workspace,
-                            size_t workspace_bytes, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
+namespace pa {
+namespace {
+// Checks of pa_prefill_varlen's arguments and its launch arguments, the error
+// word left to the caller; a->num_tokens == 0 when there is nothing to do.
+pa_status prefill_args(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
+                       int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
+                       int32_t max_context_len, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       PrefillArgs* a) {
+  *a = PrefillArgs{};
   if (batch < 0 || num_tokens < 0 || max_seqlen_q < 0) return PA_ERR_SHAPE;
   if (batch == 0 || num_tokens == 0 || max_seqlen_q == 0) return num_tokens == 0 ? PA_OK : PA_ERR_SHAPE;
   if (num_tokens > 0x7fffffff) return PA_ERR_SHAPE;
@@ -413,38 +458,107 @@ pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int3
   if (!isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
   if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
-  cudaError_t e;
   if (workspace) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGN;
     PrefillPlan plan;
-    if ((e = plan_prefill(*desc, batch, max_seqlen_q, num_tokens, max_context_len, &plan)) != cudaSuccess)
-      return cuda_fail(e);
+    cudaError_t e = plan_prefill(*desc, batch, max_seqlen_q, num_tokens, max_context_len, &plan);
+    if (e != cudaSuccess) return cuda_fail(e);
     if (plan.ws_bytes == 0) workspace = nullptr;  // this call is never planned
     else if (workspace_bytes < plan.ws_bytes) return PA_ERR_WORKSPACE;
   }
+  a->q = q;
+  a->cu_seqlens_q = cu_seqlens_q;
+  a->k_cache = k_cache;
+  a->v_cache = v_cache;
+  a->block_tables = block_tables;
+  a->context_lens = context_lens;
+  a->out = out;
+  a->num_tokens = num_tokens;
+  a->batch = batch;
+  a->max_seqlen_q = max_seqlen_q;
+  a->max_pages = max_pages_per_seq;
+  a->max_context_len = max_context_len;
+  a->scale = scale;
+  a->workspace = workspace;
+  a->workspace_bytes = workspace_bytes;
+  return PA_OK;
+}
+
+cudaError_t launch_prefill(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s) {
+  return d.dtype == PA_BF16 && d.head_dim == 128 ? launch_prefill_tc(d, a, s) : launch_prefill_simt(d, a, s);
+}
+}  // namespace
+}  // namespace pa
+
+pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
+                            int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
+                            int32_t max_context_len, float scale, void* out, void* workspace,
+                            size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  PrefillArgs a;
+  st = prefill_args(desc, q, cu_seqlens_q, batch, max_seqlen_q, num_tokens, k_cache, v_cache, block_tables,
+                    max_pages_per_seq, context_lens, max_context_len, scale, out, workspace, workspace_bytes, &a);
+  if (st != PA_OK || a.num_tokens == 0) return st;
+  if ((st = prepare(&a.err)) != PA_OK) return st;
+  cudaError_t e = launch_prefill(*desc, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_prefill_step(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
+                          int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
+                          const int32_t* cu_seqlens_q, int32_t batch, int32_t max_seqlen_q,
+                          const int32_t* context_lens, int32_t max_context_len, const int32_t* block_tables,
+                          int32_t max_pages_per_seq, const void* q_norm_w, const void* k_norm_w, float eps,
+                          float rope_theta, float scale, void* q_out, void* k_cache, void* v_cache,
+                          int32_t* positions_out, int64_t* slot_mapping_out, void* out, void* workspace,
+                          size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0 || batch < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  const bool norm = q_norm_w != nullptr || k_norm_w != nullptr;
+  // every argument of both parts is checked before anything is enqueued
+  NormRopeParams np;
+  SlotMapParams sp;
+  KvWriteParams kp;
+  if (norm) {
+    st = prefill_norm_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, cu_seqlens_q,
+                             batch, context_lens, block_tables, max_pages_per_seq, q_norm_w, k_norm_w, eps,
+                             rope_theta, q_out, k_cache, v_cache, positions_out, slot_mapping_out, &np);
+  } else {
+    // attention reads q itself, so its rows must be packed
+    if (q_row_stride != static_cast<int64_t>(desc->num_q_heads) * desc->head_dim) return PA_ERR_SHAPE;
+    if (batch == 0 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
+    st = slot_map_params(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq, num_tokens,
+                         positions_out, slot_mapping_out, &sp);
+    if (st == PA_OK)
+      st = kv_write_params(desc, k, k_row_stride, v, v_row_stride, num_tokens, slot_mapping_out, k_cache, v_cache,
+                           &kp);
+  }
+  if (st != PA_OK) return st;
+  PrefillArgs a;
+  st = prefill_args(desc, norm ? q_out : q, cu_seqlens_q, batch, max_seqlen_q, num_tokens, k_cache, v_cache,
+                    block_tables, max_pages_per_seq, context_lens, max_context_len, scale, out, workspace,
+                    workspace_bytes, &a);
+  if (st != PA_OK) return st;
   unsigned int* err = nullptr;
   if ((st = prepare(&err)) != PA_OK) return st;
-  PrefillArgs a{};
-  a.q = q;
-  a.cu_seqlens_q = cu_seqlens_q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.out = out;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (norm) {
+    np.err = err;
+    e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, np, s);
+  } else {
+    sp.err = kp.err = err;
+    e = launch_slot_mapping(sp, s);
+    if (e == cudaSuccess) e = launch_kv_write(kp, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
   a.err = err;
-  a.num_tokens = num_tokens;
-  a.batch = batch;
-  a.max_seqlen_q = max_seqlen_q;
-  a.max_pages = max_pages_per_seq;
-  a.max_context_len = max_context_len;
-  a.scale = scale;
-  a.workspace = workspace;
-  a.workspace_bytes = workspace_bytes;
-  if (desc->dtype == PA_BF16 && desc->head_dim == 128)
-    e = launch_prefill_tc(*desc, a, static_cast<cudaStream_t>(stream));
-  else
-    e = launch_prefill_simt(*desc, a, static_cast<cudaStream_t>(stream));
+  a.planner_beside_write = true;
+  e = launch_prefill(*desc, a, s);
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

@@ -59,6 +59,9 @@ __global__ void __launch_bounds__(128) slot_mapping_kernel(const SlotMapParams p
 // one thread per chunk of K and the same chunk of V.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
+  // the prefill planner of the same step may start beside this grid (it
+  // reads none of its output and waits for it before it exits)
+  pdl_trigger();
   const uint32_t cpr = static_cast<uint32_t>(p.row_bytes) >> 4;
   const int64_t total = p.n_tokens * cpr;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -223,6 +226,7 @@ __global__ void __launch_bounds__(kNrThreads) norm_rope_kv_write_kernel(const No
   // the CTA's tokens' (position, slot) when they come from the metadata
   longlong2* meta_s = reinterpret_cast<longlong2*>(sn_s + HD / 2);
   __shared__ int abort_flag;
+  pdl_trigger();  // as in kv_write_kernel: the prefill planner may start beside this grid
 
   const int64_t t0 = blockIdx.x, dt = gridDim.x;
   const int n_mine = static_cast<int>((p.n_tokens - t0 + dt - 1) / dt);  // tokens of this CTA

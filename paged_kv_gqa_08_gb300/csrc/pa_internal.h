@@ -178,6 +178,11 @@ struct PrefillArgs {
   // q-tile pair in grid order, no split).
   void* workspace = nullptr;
   size_t workspace_bytes = 0;
+  // The stream's previous kernel is this library's KV write of the same step,
+  // launched by the same call: it reads none of the metadata's producers'
+  // output, so the planner may start beside it (and waits for it before it
+  // exits, which the attention kernel's wait on the planner then covers).
+  bool planner_beside_write = false;
 };
 // Workspace layout of the planned tensor-core prefill (byte offsets, each
 // 256-aligned); ws_bytes == 0 when the call cannot be planned.

@@ -1283,6 +1283,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
       raise_flag(q.err, PA_DEVERR_BAD_LENGTH);
       q.hdr[0] = q.hdr[1] = q.hdr[2] = q.hdr[3] = q.hdr[4] = 0;
     }
+    pdl_wait();  // the KV write beside which it may run has completed
     return;
   }
   const int n_pairs = static_cast<int>(carry);
@@ -1482,6 +1483,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     q.hdr[3] = n_pairs;
     q.hdr[4] = 0;  // the attention kernel's work counter
   }
+  pdl_wait();  // the KV write beside which it may run has completed
 }
 
 // ---------------------------------------------------------------------------
@@ -1736,11 +1738,21 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   q.split_cap = pl.run_split_cap;
   // part sizes are scored only when the call may split (when its tokens
   // alone make pairs that fill more than kSplitWaves waves it may not)
-  if (q.slot_cap > 1)
-    prefill_plan_kernel<true><<<1, kPlanThreads, plan_dyn_bytes(pl.n_sm), s>>>(q);
-  else
-    prefill_plan_kernel<false><<<1, kPlanThreads, 0, s>>>(q);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The planner reads only the varlen metadata.  Behind the same call's KV
+  // write (which writes none of it) it is launched to run beside that kernel;
+  // it waits for it before it exits, so the attention kernel's wait on the
+  // planner is a wait on both.  Otherwise it starts after the previous kernel.
+  {
+    void* args[] = {&q};
+    const void* fn = q.slot_cap > 1 ? reinterpret_cast<const void*>(prefill_plan_kernel<true>)
+                                    : reinterpret_cast<const void*>(prefill_plan_kernel<false>);
+    const size_t dyn = q.slot_cap > 1 ? plan_dyn_bytes(pl.n_sm) : 0;
+    if (a.planner_beside_write)
+      e = launch_after_previous(fn, dim3(1), dim3(kPlanThreads), dyn, s, args);
+    else
+      e = cudaLaunchKernel(fn, dim3(1), dim3(kPlanThreads), args, dyn, s);
+    if (e != cudaSuccess) return e;
+  }
 
   p.units = q.units;
   p.n_units = q.hdr;

@@ -13,7 +13,7 @@ from typing import Optional
 
 import torch
 
-from . import (pa_decode, pa_decode_workspace_size, pa_kv_write, pa_prefill_qk_norm_rope_kv_write, pa_prefill_varlen,
+from . import (pa_decode, pa_decode_workspace_size, pa_kv_write, pa_prefill_qk_norm_rope_kv_write, pa_prefill_step,
                pa_prefill_workspace_size, pa_slot_mapping)
 
 
@@ -76,8 +76,14 @@ def run_step(desc, kind: str, bufs: StepBuffers, q, k, v, cu_seqlens_q, context_
     """Run one step; returns ``bufs.out`` (the attention output of the new tokens)."""
     n = q.shape[0]
     batch = context_lens.shape[0]
-    q_row = desc.num_q_heads * desc.head_dim
-    kv_row = desc.num_kv_heads * desc.head_dim
+    if kind != "decode":
+        # the write part and the attention in one call, whose attention planner
+        # runs beside the write kernel
+        pa_prefill_step(desc, q, q.stride(0), k, k.stride(0), v, v.stride(0), n, cu_seqlens_q, batch, max_seqlen_q,
+                        context_lens, max_context_len, block_tables, max_pages_per_seq, q_norm_w, k_norm_w, eps,
+                        rope_theta, scale, bufs.q_out, k_cache, v_cache, bufs.positions, bufs.slots, bufs.out,
+                        bufs.workspace, stream=stream)
+        return bufs.out
     if q_norm_w is not None:
         # slot mapping, norm, rotary and KV write in one kernel
         pa_prefill_qk_norm_rope_kv_write(desc, q, q.stride(0), k, k.stride(0), v, v.stride(0), n, cu_seqlens_q,
@@ -90,12 +96,6 @@ def run_step(desc, kind: str, bufs: StepBuffers, q, k, v, cu_seqlens_q, context_
                         bufs.slots, stream)
         pa_kv_write(desc, k, k.stride(0), v, v.stride(0), n, bufs.slots, k_cache, v_cache, stream)
         qa = q
-    assert q_row > 0 and kv_row > 0
-    if kind == "decode":
-        pa_decode(desc, qa, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens,
-                  max_context_len, scale, bufs.max_ctas, bufs.out, bufs.workspace, None, stream)
-    else:
-        pa_prefill_varlen(desc, qa, cu_seqlens_q, batch, max_seqlen_q, n, k_cache, v_cache, block_tables,
-                          max_pages_per_seq, context_lens, max_context_len, scale, bufs.out, bufs.workspace,
-                          stream=stream)
+    pa_decode(desc, qa, batch, k_cache, v_cache, block_tables, max_pages_per_seq, context_lens, max_context_len,
+              scale, bufs.max_ctas, bufs.out, bufs.workspace, None, stream)
     return bufs.out

@@ -160,6 +160,30 @@ def test_prefill_argument_validation(lib):
                                  FAKE, None, 0, None) == pa.PA_ERR_SHAPE       # the scale must be positive
 
 
+def test_prefill_step_argument_validation(lib):
+    d = _desc()
+
+    def call(n=100, batch=2, maxq=64, q_stride=16 * 128, qw=FAKE, kw=FAKE, q_out=FAKE, pos=FAKE, slots=FAKE,
+             max_ctx=128, maxp=8, scale=0.1, ws=None):
+        return lib.pa_prefill_step(ctypes.byref(d), FAKE, q_stride, FAKE, 8 * 128, FAKE, 8 * 128, n, FAKE, batch,
+                                   maxq, FAKE, max_ctx, FAKE, maxp, qw, kw, 1e-6, 1e6, scale, q_out, FAKE, FAKE, pos,
+                                   slots, FAKE, ws, 0 if ws is None else 1 << 20, None)
+
+    assert call(n=0) == pa.PA_OK
+    assert call(n=0, batch=0, qw=None) == pa.PA_OK           # nothing to do: nothing checked past the sizes
+    assert call(n=-1) == pa.PA_ERR_SHAPE
+    assert call(batch=0) == pa.PA_ERR_SHAPE                  # tokens without requests
+    assert call(kw=None) == pa.PA_ERR_NULL                   # one norm weight alone
+    assert call(q_out=None) == pa.PA_ERR_NULL                # the normed q has nowhere to go
+    assert call(qw=None, kw=None, pos=None) == pa.PA_ERR_NULL    # plain write: positions and slots needed
+    assert call(qw=None, kw=None, slots=None) == pa.PA_ERR_NULL
+    assert call(qw=None, kw=None, q_stride=16 * 128 + 8) == pa.PA_ERR_SHAPE   # plain: attention reads q packed
+    assert call(maxq=200) == pa.PA_ERR_SHAPE                 # the attention part's checks come first too
+    assert call(max_ctx=200) == pa.PA_ERR_SHAPE
+    assert call(scale=-1.0) == pa.PA_ERR_SHAPE
+    assert call(ws=FAKE + 16) == pa.PA_ERR_ALIGN
+
+
 def test_prefill_workspace_size_is_zero_when_unused(lib):
     # fp32 and head_dim 64 run on the CUDA-core kernel, which takes no workspace
     assert lib.pa_prefill_workspace_size(ctypes.byref(_desc(dtype=pa.PA_F32)), 2, 64, 100, 128) == 0

@@ -6,7 +6,8 @@ import torch
 import oracle
 import synth
 from gpu_harness import GpuCase, as_f64
-from paged_kv_gqa_08_gb300 import pa_prefill_varlen, pa_prefill_workspace_size, pa_read_device_errors
+from paged_kv_gqa_08_gb300 import (pa_kv_write, pa_prefill_qk_norm_rope_kv_write, pa_prefill_varlen,
+                                   pa_prefill_workspace_size, pa_read_device_errors, pa_slot_mapping)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
@@ -275,3 +276,67 @@ def test_prefill_page_permutation_is_bitwise_invariant(case, planned):
     n = wl.num_new_tokens
     assert torch.equal(out1[:n].view(torch.int16), out2[:n].view(torch.int16))
     assert pa_read_device_errors(reset=True) == 0
+
+
+def _separate_calls(run):
+    """The prefill step as the calls pa_prefill_step is defined by, one after another."""
+    wl, t, b = run.wl, run.t, run.bufs
+    n = wl.num_new_tokens
+    if t["q_norm_w"] is not None:
+        pa_prefill_qk_norm_rope_kv_write(run.desc, t["q"], t["q"].stride(0), t["k_new"], t["k_new"].stride(0),
+                                         t["v_new"], t["v_new"].stride(0), n, t["cu_seqlens_q"], wl.batch,
+                                         t["context_lens"], t["block_tables"], wl.max_pages_per_seq, t["q_norm_w"],
+                                         t["k_norm_w"], wl.eps, wl.rope_theta, b.q_out, run.k_cache, run.v_cache,
+                                         b.positions, b.slots)
+        qa = b.q_out
+    else:
+        pa_slot_mapping(run.desc, wl.batch, t["cu_seqlens_q"], t["context_lens"], t["block_tables"],
+                        wl.max_pages_per_seq, n, b.positions, b.slots)
+        pa_kv_write(run.desc, t["k_new"], t["k_new"].stride(0), t["v_new"], t["v_new"].stride(0), n, b.slots,
+                    run.k_cache, run.v_cache)
+        qa = t["q"]
+    pa_prefill_varlen(run.desc, qa, t["cu_seqlens_q"], wl.batch, max(wl.max_new_len, 1), n, run.k_cache, run.v_cache,
+                      t["block_tables"], wl.max_pages_per_seq, t["context_lens"], max(wl.max_context_len, 1),
+                      wl.scale, b.out, b.workspace)
+    return b.out
+
+
+STEP_CASES = [
+    ("qwen3_0p6b_chunked_prefill", True),
+    ("qwen3_0p6b_chunked_prefill", False),
+    ("prefill_2k", True),
+    (dict(kind="prefill", dtype="bf16", B=4, Hq=16, Hkv=4, hd=128, P=16, chunks=[300, 1, 45, 129],
+          prefixes=[2000, 70, 0, 513], norm=False, seed=41), True),          # plain: slot mapping + KV write
+    (dict(kind="prefill", dtype="f32", B=3, Hq=4, Hkv=2, hd=64, P=16, chunks=[1, 9, 33],
+          prefixes=[0, 16, 5], norm=True, seed=50), True),                   # CUDA-core attention
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=[f"{c[0] if isinstance(c[0], str) else c[0]['dtype'] + '-' + ('norm' if c[0]['norm'] else 'plain')}-{'planned' if c[1] else 'unplanned'}" for c in STEP_CASES])
+def test_prefill_step_equals_the_separate_calls(case):
+    """pa_prefill_step (its planner beside the write kernel) gives exactly the
+    cache, positions, slots, q_out and output of the separate calls."""
+    name, planned = case
+    wl = synth.make_workload(name)
+    runs = [GpuCase(wl, plan_prefill=planned), GpuCase(wl, plan_prefill=planned)]
+    outs = []
+    for k, run in enumerate(runs):
+        run.bufs.out.fill_(0)
+        run.bufs.positions.fill_(-5)
+        run.bufs.slots.fill_(-5)
+        pa_read_device_errors(reset=True)
+        outs.append(run.step() if k == 0 else _separate_calls(run))
+        torch.cuda.synchronize()
+        assert pa_read_device_errors(reset=True) == 0
+    a, b = runs
+    n = wl.num_new_tokens
+
+    def bits(x):
+        return x.contiguous().view(-1).view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32)
+    assert torch.equal(bits(outs[0]), bits(outs[1]))
+    assert torch.equal(a.bufs.positions[:n], b.bufs.positions[:n])
+    assert torch.equal(a.bufs.slots[:n], b.bufs.slots[:n])
+    if wl.q_norm_w is not None:
+        assert torch.equal(bits(a.bufs.q_out[:n]), bits(b.bufs.q_out[:n]))
+    assert torch.equal(bits(a.k_cache), bits(b.k_cache)) and torch.equal(bits(a.v_cache), bits(b.v_cache))
+    _check(outs[0][:n], oracle.reference_step(wl)["o"], wl.dtype)
