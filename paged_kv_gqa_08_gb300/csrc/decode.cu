@@ -46,6 +46,7 @@ constexpr int kStages = 3;       // shared-memory ring depth (CUDA-core consumer
 constexpr int kStagesMma = 3;    // ring depth of the tensor-core consumers (one CTA per SM)
 constexpr int kMmaTok = 16;      // tokens per chunk of the tensor-core consumers
 constexpr int kPlanThreads = 1024;
+constexpr int kInlinePlanMax = 512;  // batches the decode CTAs plan themselves (else a plan kernel runs first)
 constexpr int kMergeThreads = 128;
 
 __host__ __device__ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
@@ -81,6 +82,8 @@ struct KParams {
   int32_t row_pitch;    // shared-memory bytes per token row of a stage (row_bytes, + 16 for the MMA consumers)
   int32_t chunk_bytes;  // T * row_pitch
   uint32_t off_bar, off_meta, off_p, off_alpha, off_ml, off_abort;
+  uint32_t off_cs;      // [kInlinePlanMax + 1] chunk prefix sums, then [32] warp totals (inline plan)
+  int32_t inline_plan;  // 1: no plan kernel ran; every CTA computes the prefix sums itself
   int32_t p_row;        // floats per token row of the probability tile
   float scale_log2;     // softmax scale * log2(e)
   int32_t merge_w;      // warps per (request, q-head) in the merge kernel: 1, 2 or 4
@@ -92,6 +95,16 @@ struct KParams {
   int64_t k_new_stride, v_new_stride;  // bytes
   int64_t* slot_out;                   // optional: the slot written for request b
 };
+
+// First request whose chunks extend past chunk x0 (cs: the prefix sums).
+__device__ __forceinline__ int first_request(const int32_t* cs, int B, int64_t x0) {
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cs[mid + 1] > x0) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
 
 // ---------------------------------------------------------------------------
 // plan: chunk prefix sums and each CTA's first request
@@ -145,15 +158,63 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const KParams
   if (tid == 0) p.cs[0] = 0;
   cta_sync();
   const int NC = carry;
-  for (int c = tid; c < p.n_ctas; c += kPlanThreads) {
-    const int64_t x0 = (static_cast<int64_t>(c) * NC) / p.n_ctas;
-    int lo = 0, hi = p.B;  // first request whose chunks extend past x0
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (p.cs[mid + 1] > x0) hi = mid; else lo = mid + 1;
+  for (int c = tid; c < p.n_ctas; c += kPlanThreads)
+    p.cta_seq[c] = first_request(p.cs, p.B, (static_cast<int64_t>(c) * NC) / p.n_ctas);
+}
+
+// The plan kernel's prefix sums, computed by every thread of a decode CTA into
+// its shared memory (B <= kInlinePlanMax): each thread sums the chunk counts
+// of a run of consecutive requests, the runs' totals are scanned across the
+// CTA, then each thread writes its run's prefix sums.  CTA 0 also does the
+// plan kernel's side work: it publishes the sums for the merge kernel, flags
+// bad lengths and marks the slots of rows it skips.
+__device__ __forceinline__ void plan_in_cta(const KParams& p, int32_t* cs_s, int32_t* warp_tot, bool first) {
+  const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = 1 << p.log2T;
+  const int cap = static_cast<int>(min(static_cast<int64_t>(p.max_ctx), static_cast<int64_t>(p.maxp) << p.log2P));
+  const int per = (p.B + nthr - 1) / nthr;
+  const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int L = p.ctx[b];
+    int cnt = 0;
+    if (L >= 1 && L <= cap) {
+      cnt = (L + T - 1) >> p.log2T;
+    } else if (first) {
+      // length 0 is a padding row: nothing is read, stored or written for it
+      if (L != 0) raise_flag(p.err, PA_DEVERR_BAD_LENGTH);
+      if (p.k_new != nullptr && p.slot_out) p.slot_out[b] = -1;
     }
-    p.cta_seq[c] = lo;
+    cs_s[b + 1] = cnt;
+    sum += cnt;
   }
+  int x = sum;  // inclusive scan of the runs' totals: within the warp, then over the warps
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  cta_sync();
+  if (warp == 0) {
+    int w = lane < (nthr >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w;
+  }
+  cta_sync();
+  int run = x - sum + (warp ? warp_tot[warp - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    run += cs_s[b + 1];
+    cs_s[b + 1] = run;
+  }
+  if (tid == 0) cs_s[0] = 0;
+  cta_sync();
+  if (first)
+    for (int b = tid; b <= p.B; b += nthr) p.cs[b] = cs_s[b];
 }
 
 // ---------------------------------------------------------------------------
@@ -465,9 +526,17 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD,
   const int NW = p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  pdl_wait();     // the plan kernel's chunk sums and CTA starts are complete
+  const int32_t* cs;  // [B+1] chunk prefix sums
+  if (p.inline_plan) {
+    int32_t* cs_s = reinterpret_cast<int32_t*>(smem + p.off_cs);
+    plan_in_cta(p, cs_s, cs_s + kInlinePlanMax + 1, c == 0);
+    cs = cs_s;
+  } else {
+    pdl_wait();  // the plan kernel's chunk sums and CTA starts are complete
+    cs = p.cs;
+  }
   pdl_trigger();  // the merge kernel may start launching; it waits for this grid
-  const int NC = p.cs[p.B];
+  const int NC = cs[p.B];
   const int x0 = static_cast<int>((static_cast<int64_t>(c) * NC) / p.n_ctas);
   const int x1 = static_cast<int>((static_cast<int64_t>(c + 1) * NC) / p.n_ctas);
   if (x0 >= x1) return;
@@ -492,7 +561,7 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD,
     // ------------------------------ producer ------------------------------
     const uint64_t pol = l2_policy_evict_first();
     const int tok = 1 << p.log2T;
-    int b = p.cta_seq[c];
+    int b = p.inline_plan ? first_request(cs, p.B, x0) : p.cta_seq[c];
     int issued = 0;
     bool aborted = false;
     for (int xg = x0; xg < x1 && !aborted; xg += 32) {
@@ -501,8 +570,8 @@ __global__ void __launch_bounds__(9 * 32) __maxnreg__((G <= 4 && !kUseMma<T, HD,
       int my_b = b, n = 0, flags = 0, new_slot = -1;
       long long off = 0;
       if (lane < nvalid) {
-        while (my_b < p.B - 1 && p.cs[my_b + 1] <= x) ++my_b;
-        const int cb0 = p.cs[my_b], cb1 = p.cs[my_b + 1];
+        while (my_b < p.B - 1 && cs[my_b + 1] <= x) ++my_b;
+        const int cb0 = cs[my_b], cb1 = cs[my_b + 1];
         const int jc = x - cb0;
         const int t0 = jc << p.log2T;
         n = min(tok, p.ctx[my_b] - t0);
@@ -1016,6 +1085,10 @@ cudaError_t plan_decode(const pa_cache_desc& d, int batch, int max_ctx, int max_
   off += static_cast<size_t>(pl.nw) * 8 * 4;
   pl.off_ml = static_cast<uint32_t>(off);
   off += static_cast<size_t>(pl.nw) * 16 * 4;
+  // room for the batch's prefix sums (whatever the batch, so that the CTAs
+  // per SM, and with them the plan, do not depend on it)
+  pl.off_cs = static_cast<uint32_t>(align_up(off, 16));
+  off = pl.off_cs + static_cast<size_t>(kInlinePlanMax + 1 + 32) * 4;
   pl.smem_bytes = align_up(off, 128);
   if (pl.smem_bytes > static_cast<size_t>(di.max_smem_optin)) return cudaErrorInvalidValue;
   int occ = 0;
@@ -1080,6 +1153,8 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   p.off_alpha = pl.off_alpha;
   p.off_ml = pl.off_ml;
   p.off_abort = pl.off_abort;
+  p.off_cs = pl.off_cs;
+  p.inline_plan = a.batch <= kInlinePlanMax ? 1 : 0;
   p.p_row = pl.p_row;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.k_new = static_cast<const char*>(a.k_new);
@@ -1088,13 +1163,21 @@ cudaError_t launch_decode(const pa_cache_desc& d, const DecodePlan& pl, const De
   p.v_new_stride = a.v_new_stride_bytes;
   p.slot_out = a.slot_out;
 
-  // plan -> decode -> merge, the last two launched to overlap their launch with
-  // the kernel before them (each waits for it before reading its output)
-  decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // (plan ->) decode -> merge.  Up to kInlinePlanMax requests every decode CTA
+  // computes the plan's prefix sums itself, which costs less than a kernel
+  // boundary on the step's critical path; beyond, a plan kernel runs first.
+  // The kernels after the first are launched to overlap their launch with the
+  // kernel before them (each waits for it before reading its output).
   void* args[] = {&p};
-  e = launch_after_previous(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), pl.smem_bytes, s, args);
+  cudaError_t e;
+  if (p.inline_plan) {
+    e = cudaLaunchKernel(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), args, pl.smem_bytes, s);
+  } else {
+    decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_after_previous(f.main, dim3(pl.n_ctas), dim3((pl.nw + 1) * 32), pl.smem_bytes, s, args);
+  }
   if (e != cudaSuccess) return e;
   if (pl.n_ctas > 1) {
     // warps per (request, q-head): about one per 8 partials of a request when

@@ -114,6 +114,7 @@ struct DecodePlan {
   size_t ws_cs = 0, ws_cta_seq = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
   // shared-memory layout (byte offsets)
   uint32_t off_bar = 0, off_meta = 0, off_p = 0, off_alpha = 0, off_ml = 0, off_abort = 0;
+  uint32_t off_cs = 0;   // the batch's chunk prefix sums when each CTA plans for itself
   int p_row = 0;         // floats per token row of the probability tile
 };
 // Plan for the current device; returns cudaErrorInvalidValue for an

@@ -8,7 +8,7 @@ import torch
 import oracle
 import synth
 from gpu_harness import GpuCase, as_f64, storage
-from paged_kv_gqa_08_gb300 import PA_DEVERR_BAD_LENGTH, pa_decode_kv_write, pa_read_device_errors
+from paged_kv_gqa_08_gb300 import PA_DEVERR_BAD_LENGTH, pa_decode, pa_decode_kv_write, pa_read_device_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
@@ -85,6 +85,35 @@ def test_fused_decode_reports_skipped_requests():
     assert np.array_equal(s[good], ref["slots"][good])
     ok, err, bound = oracle.within_tolerance(as_f64(out[good]), ref["o"][good], wl.dtype)
     assert ok, (err, bound)
+
+
+@pytest.mark.parametrize("B", [512, 513, 1100])
+def test_decode_batches_on_both_sides_of_the_in_kernel_plan_limit(B):
+    """Up to 512 requests every decode CTA computes the batch's chunk prefix
+    sums itself; beyond that a plan kernel computes them first.  On both sides
+    of the limit: the fused call against the oracle (cache bit for bit), then
+    pa_decode with a padding row (skipped, no flag) and a bad length (skipped,
+    flagged) among the requests."""
+    wl = synth.make_workload(dict(kind="decode", dtype="bf16", B=B, Hq=16, Hkv=8, hd=128, P=16, L_range=(1, 96),
+                                  seed=B + 3))
+    run = GpuCase(wl)
+    pa_read_device_errors(reset=True)
+    out, slots = _fused(run, wl)
+    _check_all(run, wl, out, slots)
+    assert pa_read_device_errors(reset=True) == 0
+    ref = oracle.reference_step(wl)
+    ctx = run.t["context_lens"].clone()
+    ctx[B - 2] = 0
+    ctx[7] = -1
+    out2 = torch.full_like(run.bufs.out, 7.0)
+    pa_decode(run.desc, run.t["q"], wl.batch, run.k_cache, run.v_cache, run.t["block_tables"], wl.max_pages_per_seq,
+              ctx, wl.max_context_len, wl.scale, 0, out2, run.bufs.workspace)
+    torch.cuda.synchronize()
+    assert pa_read_device_errors(reset=True) == PA_DEVERR_BAD_LENGTH
+    good = [b for b in range(B) if b not in (7, B - 2)]
+    ok, err, bound = oracle.within_tolerance(as_f64(out2[good]), ref["o"][good], wl.dtype)
+    assert ok, (err, bound)
+    assert torch.all(out2[B - 2] == 7.0) and torch.all(out2[7] == 7.0)
 
 
 @pytest.mark.parametrize("name", ["qwen3_0p6b_decode", "long_context_decode"])
