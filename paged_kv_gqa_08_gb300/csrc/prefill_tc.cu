@@ -87,7 +87,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kOffQ = 0;                          // two q-tiles
 constexpr int kOffK = kOffQ + 2 * kTileBytes;     // two K stages
 constexpr int kOffV = kOffK + 2 * kTileBytes;     // two V stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;   // 26 mbarriers
+constexpr int kStageBytes = 32 * 128;             // a softmax warp's 32 rows x 128 bytes on their way out
+constexpr int kOffStage = kOffV + 2 * kTileBytes; // eight softmax warps' output staging (1024-aligned)
+constexpr int kOffBar = kOffStage + 8 * kStageBytes;  // 26 mbarriers
 // indices of the mbarriers in their table (pairs are [2], one per stage or group)
 constexpr int kBarItemFull = 0, kBarItemEmpty = 2, kBarQFull = 4, kBarQEmpty = 5, kBarKFull = 6, kBarKEmpty = 8,
               kBarVFull = 10, kBarVEmpty = 12, kBarSFull = 14, kBarPFull = 16, kBarPvDone = 18, kBarOFree = 20,
@@ -96,6 +98,8 @@ constexpr int kOffItem = kOffBar + 256;           // two work items
 constexpr int kOffMl = kOffItem + 256;            // 128 (max, sum) rows handed between the softmax groups
 constexpr int kOffMisc = kOffMl + 128 * 8;        // TMEM base address, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+static_assert(kSmemBytes <= 232448, "within the 227 KB a CTA may use");
+static_assert(kOffStage % 1024 == 0, "128-byte-swizzled staging starts on a 1024-byte boundary");
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, M = 128, N = 128.
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
@@ -108,6 +112,8 @@ struct TcParams {
   CUtensorMap tm_k1;   //                box {64, 1}
   CUtensorMap tm_v16;
   CUtensorMap tm_v1;
+  CUtensorMap tm_o;    // out    [num_tokens, Hq, 128], box {64, G, 32 / G}: one softmax warp's rows
+  int32_t o_tma;       // 1: tm_o is valid (G a power of two, so a warp's 32 rows are whole tokens)
   const int32_t* cu;
   const int32_t* bt;
   const int32_t* ctx;
@@ -145,6 +151,14 @@ PA_DEVINL void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z
       "[%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Shared -> global copy of a 3-D box (bulk async-group of the issuing thread).
+PA_DEVINL void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 
 PA_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -460,7 +474,44 @@ PA_DEVINL void store_cols(const uint32_t (&o)[N], float a, bool part, bool live,
   }
 }
 
+// A softmax warp's 32 output rows (whole tokens: G q-heads each), scaled by
+// a and rounded to bf16, through its 4 KB staging buffer and two TMA stores
+// of half a row each.  Chunk c (16 bytes) of row r sits at chunk c ^ (r & 7)
+// of the row's 128 bytes -- the 128-byte swizzle the tensor map names, so
+// neither these writes nor the TMA engine's reads meet a bank conflict.  The
+// warp does not wait for the global writes; before it refills the buffer,
+// lane 0 (whose bulk groups these are) waits until the previous store has
+// read it.
+PA_DEVINL void store_rows_tma(const uint32_t (&o)[128], float a, uint32_t stage, const CUtensorMap* tm, int y,
+                              int z, int lane, bool& pending) {
+  auto f = [&](int e) { return __uint_as_float(o[e]) * a; };
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (pending) {
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      __syncwarp();
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int e = 64 * h + 8 * c;
+      const uint32_t addr = stage + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pack_bf16x2(f(e), f(e + 1))),
+                   "r"(pack_bf16x2(f(e + 2), f(e + 3))), "r"(pack_bf16x2(f(e + 4), f(e + 5))),
+                   "r"(pack_bf16x2(f(e + 6), f(e + 7)))
+                   : "memory");
+    }
+    fence_async_smem();  // the rows are visible to the TMA engine
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tm, stage, 64 * h, y, z);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    pending = true;
+  }
+}
+
 struct SoftmaxArgs {
+  const CUtensorMap* tm_o;  // output rows by TMA (null: by the threads' own stores)
   char* out;
   bool out32;  // out is 32-byte aligned (whole-sector stores)
   float* o_part;
@@ -499,6 +550,8 @@ __device__ __noinline__ void softmax_role(const SoftmaxArgs p, unsigned char* sm
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t colS = g * 128, colO = 256 + g * 128;
   const int t_r = row / p.G, gg = row - (row / p.G) * p.G;
+  const uint32_t stage = smem_u32(smem + kOffStage + warp * kStageBytes);
+  bool tma_pending = false;  // this warp has output stores in flight
   int sc = 0;          // S tiles this group has consumed
   int pc[2] = {0, 0};  // PVs issued per group before the current item
   int ms = 0;          // split-mode items done
@@ -633,7 +686,10 @@ __device__ __noinline__ void softmax_role(const SoftmaxArgs p, unsigned char* sm
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free[g]);
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        store_cols<0>(o, inv, slot >= 0, live, p.o_part + prow * 128, dst, p.out32);
+        if (p.tm_o != nullptr && slot < 0 && __all_sync(0xffffffffu, live))
+          store_rows_tma(o, inv, stage, p.tm_o, hh_kv * p.G, it_s0 + qt * p.TQ + wq * 32 / p.G, lane, tma_pending);
+        else
+          store_cols<0>(o, inv, slot >= 0, live, p.o_part + prow * 128, dst, p.out32);
         if (slot >= 0) p.lse_part[prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
       } else if (slot >= 0) {
         p.lse_part[prow] = -INFINITY;  // no key tile of this part reaches the q-tile
@@ -703,6 +759,8 @@ __device__ __noinline__ void softmax_role(const SoftmaxArgs p, unsigned char* sm
       ++ms;
     }
   }
+  // the output stores have completed (and read their staging) before the CTA exits
+  if (tma_pending && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
@@ -787,6 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (warp < kKWarp) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     SoftmaxArgs sa;
+    sa.tm_o = p.o_tma ? &p.tm_o : nullptr;
     sa.out = p.out;
     sa.out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
     sa.o_part = p.o_part;
@@ -1648,6 +1707,12 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
     const cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(d.num_q_heads) * 256};
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(TQ)};
     if (!encode(fn, &p.tm_q, a.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    // output rows by TMA when a softmax warp's 32 rows are whole tokens
+    if ((G & (G - 1)) == 0) {
+      const cuuint32_t obox[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(32 / G)};
+      if (!encode(fn, &p.tm_o, a.out, 3, dims, strides, obox)) return cudaErrorInvalidValue;
+      p.o_tma = 1;
+    }
   }
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.num_kv_heads) * 128,
