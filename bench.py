@@ -629,7 +629,8 @@ def run_reference(args, rank, world):
 def run_case(spec: str):
     """Profiling helper: set up the first B requests of a workload and run three
     steps through the C ABI (no timing), e.g. --case decode:qwen3_8b_decode:16;
-    kind "fused" runs the decode step as pa_decode_kv_write."""
+    kind "fused" runs the decode step as pa_decode_kv_write, a prefill step is
+    one pa_prefill_step call."""
     kind, name, nreq = spec.split(":")
     nreq = int(nreq)
     fused = kind == "fused"
@@ -647,8 +648,11 @@ def run_case(spec: str):
     load_library()
     d = Device(wl, "cuda:0", fused=fused)
     for _ in range(3):
-        d.write_part()
-        d.attn_part()
+        if wl.kind == "prefill":
+            d.prefill_step()
+        else:
+            d.write_part()
+            d.attn_part()
     torch.cuda.synchronize()
     print(json.dumps({"case": spec, "workload": describe(wl), "kv_bytes": kv_bytes(wl),
                       "decode_bytes": decode_call_bytes(wl) if wl.kind == "decode" else None,
