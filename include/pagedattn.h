@@ -35,6 +35,14 @@
  * Supported: dtype fp32 or bf16; head_dim 64 or 128; num_kv_heads a power of
  * two <= 8; group size num_q_heads / num_kv_heads in 1..8; page_size a power
  * of two >= 16.  All vector pointers and row strides must be 16-byte aligned.
+ *
+ * Stream order: each call's first kernel starts after the stream's previous
+ * work has completed.  The KV-write kernels (pa_kv_write and the two norm /
+ * rotary writes) allow programmatically dependent kernels to launch at their
+ * start (griddepcontrol.launch_dependents): a kernel the caller enqueues
+ * after them with programmatic stream serialisation must wait
+ * (griddepcontrol.wait, cudaGridDependencySynchronize) before it reads what
+ * they write -- as the CUDA programming model asks of any such kernel.
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H

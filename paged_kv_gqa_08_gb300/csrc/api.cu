@@ -119,12 +119,9 @@ cudaError_t device_error_word(unsigned int** out) {
 
 }  // namespace pa
 
-using namespace pa;
-
-extern "C" {
-
 namespace pa {
 namespace {
+
 // Checks of pa_slot_mapping's arguments (batch > 0) and its parameters, the
 // error word left to the caller.
 pa_status slot_map_params(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
@@ -171,42 +168,7 @@ pa_status kv_write_params(const pa_cache_desc* desc, const void* k, int64_t k_ro
   p.row_bytes = static_cast<int32_t>(re * E);
   return PA_OK;
 }
-}  // namespace
-}  // namespace pa
 
-pa_status pa_slot_mapping(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
-                          const int32_t* context_lens, const int32_t* block_tables, int32_t max_pages_per_seq,
-                          int64_t num_tokens, int32_t* positions, int64_t* slot_mapping, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (batch < 0 || num_tokens < 0 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
-  if (batch == 0) return num_tokens == 0 ? PA_OK : PA_ERR_SHAPE;
-  SlotMapParams p;
-  st = slot_map_params(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq, num_tokens,
-                       positions, slot_mapping, &p);
-  if (st != PA_OK) return st;
-  if ((st = prepare(&p.err)) != PA_OK) return st;
-  cudaError_t e = launch_slot_mapping(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : cuda_fail(e);
-}
-
-pa_status pa_kv_write(const pa_cache_desc* desc, const void* k, int64_t k_row_stride, const void* v,
-                      int64_t v_row_stride, int64_t num_tokens, const int64_t* slot_mapping, void* k_cache,
-                      void* v_cache, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (num_tokens < 0) return PA_ERR_SHAPE;
-  if (num_tokens == 0) return PA_OK;
-  KvWriteParams p;
-  st = kv_write_params(desc, k, k_row_stride, v, v_row_stride, num_tokens, slot_mapping, k_cache, v_cache, &p);
-  if (st != PA_OK) return st;
-  if ((st = prepare(&p.err)) != PA_OK) return st;
-  cudaError_t e = launch_kv_write(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : cuda_fail(e);
-}
-
-namespace pa {
-namespace {
 // The checks and parameters both norm / rotary entry points share; the
 // position / slot source is filled in by the caller.
 pa_status norm_rope_params(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
@@ -252,34 +214,7 @@ pa_status norm_rope_params(const pa_cache_desc* desc, const void* q, int64_t q_r
   }
   return PA_OK;
 }
-}  // namespace
-}  // namespace pa
 
-pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
-                                   int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
-                                   const int32_t* positions, const void* q_norm_w, const void* k_norm_w, float eps,
-                                   float rope_theta, const int64_t* slot_mapping, void* q_out, void* k_cache,
-                                   void* v_cache, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (num_tokens < 0) return PA_ERR_SHAPE;
-  if (num_tokens == 0) return PA_OK;
-  NormRopeParams p;
-  st = norm_rope_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, q_norm_w, k_norm_w, eps,
-                        rope_theta, q_out, k_cache, v_cache, &p);
-  if (st != PA_OK) return st;
-  if (!positions || !slot_mapping) return PA_ERR_NULL;
-  unsigned int* err = nullptr;
-  if ((st = prepare(&err)) != PA_OK) return st;
-  p.positions = positions;
-  p.slots = slot_mapping;
-  p.err = err;
-  cudaError_t e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : cuda_fail(e);
-}
-
-namespace pa {
-namespace {
 // Checks of pa_prefill_qk_norm_rope_kv_write's arguments (num_tokens > 0) and
 // its parameters, the error word left to the caller.
 pa_status prefill_norm_params(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
@@ -307,8 +242,114 @@ pa_status prefill_norm_params(const pa_cache_desc* desc, const void* q, int64_t 
   p.slots_out = slot_mapping_out;
   return PA_OK;
 }
+
+// Checks of pa_prefill_varlen's arguments and its launch arguments, the error
+// word left to the caller; a->num_tokens == 0 when there is nothing to do.
+pa_status prefill_args(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
+                       int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
+                       int32_t max_context_len, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       PrefillArgs* a) {
+  *a = PrefillArgs{};
+  if (batch < 0 || num_tokens < 0 || max_seqlen_q < 0) return PA_ERR_SHAPE;
+  if (batch == 0 || num_tokens == 0 || max_seqlen_q == 0) return num_tokens == 0 ? PA_OK : PA_ERR_SHAPE;
+  if (num_tokens > 0x7fffffff) return PA_ERR_SHAPE;
+  if (max_pages_per_seq < 1 || max_context_len < 1 || max_seqlen_q > max_context_len) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * desc->page_size)
+    return PA_ERR_SHAPE;
+  if (!isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
+  if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGN;
+    PrefillPlan plan;
+    cudaError_t e = plan_prefill(*desc, batch, max_seqlen_q, num_tokens, max_context_len, &plan);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (plan.ws_bytes == 0) workspace = nullptr;  // this call is never planned
+    else if (workspace_bytes < plan.ws_bytes) return PA_ERR_WORKSPACE;
+  }
+  a->q = q;
+  a->cu_seqlens_q = cu_seqlens_q;
+  a->k_cache = k_cache;
+  a->v_cache = v_cache;
+  a->block_tables = block_tables;
+  a->context_lens = context_lens;
+  a->out = out;
+  a->num_tokens = num_tokens;
+  a->batch = batch;
+  a->max_seqlen_q = max_seqlen_q;
+  a->max_pages = max_pages_per_seq;
+  a->max_context_len = max_context_len;
+  a->scale = scale;
+  a->workspace = workspace;
+  a->workspace_bytes = workspace_bytes;
+  return PA_OK;
+}
+
+cudaError_t launch_prefill(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s) {
+  return d.dtype == PA_BF16 && d.head_dim == 128 ? launch_prefill_tc(d, a, s) : launch_prefill_simt(d, a, s);
+}
+
 }  // namespace
 }  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+pa_status pa_slot_mapping(const pa_cache_desc* desc, int32_t batch, const int32_t* cu_seqlens_q,
+                          const int32_t* context_lens, const int32_t* block_tables, int32_t max_pages_per_seq,
+                          int64_t num_tokens, int32_t* positions, int64_t* slot_mapping, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (batch < 0 || num_tokens < 0 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
+  if (batch == 0) return num_tokens == 0 ? PA_OK : PA_ERR_SHAPE;
+  SlotMapParams p;
+  st = slot_map_params(desc, batch, cu_seqlens_q, context_lens, block_tables, max_pages_per_seq, num_tokens,
+                       positions, slot_mapping, &p);
+  if (st != PA_OK) return st;
+  if ((st = prepare(&p.err)) != PA_OK) return st;
+  cudaError_t e = launch_slot_mapping(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_kv_write(const pa_cache_desc* desc, const void* k, int64_t k_row_stride, const void* v,
+                      int64_t v_row_stride, int64_t num_tokens, const int64_t* slot_mapping, void* k_cache,
+                      void* v_cache, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  KvWriteParams p;
+  st = kv_write_params(desc, k, k_row_stride, v, v_row_stride, num_tokens, slot_mapping, k_cache, v_cache, &p);
+  if (st != PA_OK) return st;
+  if ((st = prepare(&p.err)) != PA_OK) return st;
+  cudaError_t e = launch_kv_write(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride, const void* k,
+                                   int64_t k_row_stride, const void* v, int64_t v_row_stride, int64_t num_tokens,
+                                   const int32_t* positions, const void* q_norm_w, const void* k_norm_w, float eps,
+                                   float rope_theta, const int64_t* slot_mapping, void* q_out, void* k_cache,
+                                   void* v_cache, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  NormRopeParams p;
+  st = norm_rope_params(desc, q, q_row_stride, k, k_row_stride, v, v_row_stride, num_tokens, q_norm_w, k_norm_w, eps,
+                        rope_theta, q_out, k_cache, v_cache, &p);
+  if (st != PA_OK) return st;
+  if (!positions || !slot_mapping) return PA_ERR_NULL;
+  unsigned int* err = nullptr;
+  if ((st = prepare(&err)) != PA_OK) return st;
+  p.positions = positions;
+  p.slots = slot_mapping;
+  p.err = err;
+  cudaError_t e = launch_norm_rope_kv_write(desc->dtype, desc->head_dim, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
 
 pa_status pa_prefill_qk_norm_rope_kv_write(const pa_cache_desc* desc, const void* q, int64_t q_row_stride,
                                            const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
@@ -438,57 +479,6 @@ pa_status pa_decode_kv_write(const pa_cache_desc* desc, const void* q, const voi
   e = launch_decode(*desc, pl, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
-
-namespace pa {
-namespace {
-// Checks of pa_prefill_varlen's arguments and its launch arguments, the error
-// word left to the caller; a->num_tokens == 0 when there is nothing to do.
-pa_status prefill_args(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
-                       int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
-                       const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* context_lens,
-                       int32_t max_context_len, float scale, void* out, void* workspace, size_t workspace_bytes,
-                       PrefillArgs* a) {
-  *a = PrefillArgs{};
-  if (batch < 0 || num_tokens < 0 || max_seqlen_q < 0) return PA_ERR_SHAPE;
-  if (batch == 0 || num_tokens == 0 || max_seqlen_q == 0) return num_tokens == 0 ? PA_OK : PA_ERR_SHAPE;
-  if (num_tokens > 0x7fffffff) return PA_ERR_SHAPE;
-  if (max_pages_per_seq < 1 || max_context_len < 1 || max_seqlen_q > max_context_len) return PA_ERR_SHAPE;
-  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_pages_per_seq) * desc->page_size)
-    return PA_ERR_SHAPE;
-  if (!isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
-  if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
-  if (workspace) {
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_ALIGN;
-    PrefillPlan plan;
-    cudaError_t e = plan_prefill(*desc, batch, max_seqlen_q, num_tokens, max_context_len, &plan);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (plan.ws_bytes == 0) workspace = nullptr;  // this call is never planned
-    else if (workspace_bytes < plan.ws_bytes) return PA_ERR_WORKSPACE;
-  }
-  a->q = q;
-  a->cu_seqlens_q = cu_seqlens_q;
-  a->k_cache = k_cache;
-  a->v_cache = v_cache;
-  a->block_tables = block_tables;
-  a->context_lens = context_lens;
-  a->out = out;
-  a->num_tokens = num_tokens;
-  a->batch = batch;
-  a->max_seqlen_q = max_seqlen_q;
-  a->max_pages = max_pages_per_seq;
-  a->max_context_len = max_context_len;
-  a->scale = scale;
-  a->workspace = workspace;
-  a->workspace_bytes = workspace_bytes;
-  return PA_OK;
-}
-
-cudaError_t launch_prefill(const pa_cache_desc& d, const PrefillArgs& a, cudaStream_t s) {
-  return d.dtype == PA_BF16 && d.head_dim == 128 ? launch_prefill_tc(d, a, s) : launch_prefill_simt(d, a, s);
-}
-}  // namespace
-}  // namespace pa
 
 pa_status pa_prefill_varlen(const pa_cache_desc* desc, const void* q, const int32_t* cu_seqlens_q, int32_t batch,
                             int32_t max_seqlen_q, int64_t num_tokens, const void* k_cache, const void* v_cache,
