@@ -22,7 +22,9 @@
 // writes O / l and the row log-sum-exp in fp32 for a merge kernel that
 // combines the parts of each split pair (flash-decoding's split-KV rule,
 // applied to prefill rows).  Without a workspace, each CTA runs its own
-// pair's item with all its keys.
+// pair's item with all its keys.  Launched by the prefill step right after its
+// KV-write kernel, the planner starts beside that kernel (it reads only the
+// varlen metadata) and waits for it before it exits.
 //
 // Warp roles (12 warps):
 //   warps 0-7  two softmax groups of 4 warps, one thread per row (= TMEM
@@ -32,7 +34,10 @@
 //              probabilities are written back over S's first 64 columns,
 //              where the PV MMA reads its A operand.  At an item's end O / l
 //              goes to global memory (O is released to the next item as soon
-//              as it is in registers).
+//              as it is in registers): a warp whose 32 rows are whole tokens
+//              stages them in shared memory and lane 0 issues TMA stores, so
+//              the warp does not wait on its stores; other rows are stored
+//              by their threads.
 //   warp 8     TMA producer of Q and K: an item's Q tiles (3-D map), then
 //              per 128-key tile the K rows gathered page by page with 16-row
 //              boxes (single-row boxes for a ragged end, so no slot past the
