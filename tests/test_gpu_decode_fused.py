@@ -155,3 +155,36 @@ def test_unfused_decode_with_q_and_out_in_pinned_host_memory():
     ok, err, bound = oracle.within_tolerance(as_f64(out_host[: wl.batch]), ref["o"], wl.dtype)
     assert ok, (err, bound)
     assert pa_read_device_errors(reset=True) == 0
+
+
+def test_decode_output_only_16_byte_aligned():
+    """pa_decode and pa_decode_kv_write with output rows 16 bytes past a
+    32-byte boundary give the bytes of the same call with an aligned output."""
+    wl = synth.make_workload("qwen3_0p6b_decode", B=24)
+    run = GpuCase(wl)
+    _fused(run, wl)  # the new rows are in the cache from here on: both calls below see the same keys
+    shape = tuple(run.bufs.out.shape)
+    row = wl.num_kv_heads * wl.head_dim
+    slots = torch.empty(wl.batch, dtype=torch.int64, device="cuda")
+
+    def call(fused, out):
+        if fused:  # writing the new rows again stores the same bytes
+            pa_decode_kv_write(run.desc, run.t["q"], run.t["k_new"], row, run.t["v_new"], row, wl.batch, run.k_cache,
+                               run.v_cache, run.t["block_tables"], wl.max_pages_per_seq, run.t["context_lens"],
+                               wl.max_context_len, wl.scale, 0, slots, out, run.bufs.workspace)
+        else:
+            pa_decode(run.desc, run.t["q"], wl.batch, run.k_cache, run.v_cache, run.t["block_tables"],
+                      wl.max_pages_per_seq, run.t["context_lens"], wl.max_context_len, wl.scale, 0, out,
+                      run.bufs.workspace)
+        torch.cuda.synchronize()
+
+    for fused in (True, False):
+        aligned = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        call(fused, aligned)
+        buf = torch.zeros(run.bufs.out.numel() + 8, dtype=torch.bfloat16, device="cuda")
+        out = buf[8:].view(shape)
+        assert out.data_ptr() % 32 == 16
+        call(fused, out)
+        assert torch.equal(out[:wl.batch].view(torch.int16), aligned[:wl.batch].view(torch.int16)), fused
+        assert torch.all(buf[:8].view(torch.int16) == 0)
+    assert pa_read_device_errors(reset=True) == 0

@@ -340,3 +340,28 @@ def test_prefill_step_equals_the_separate_calls(case):
         assert torch.equal(bits(a.bufs.q_out[:n]), bits(b.bufs.q_out[:n]))
     assert torch.equal(bits(a.k_cache), bits(b.k_cache)) and torch.equal(bits(a.v_cache), bits(b.v_cache))
     _check(outs[0][:n], oracle.reference_step(wl)["o"], wl.dtype)
+
+
+@pytest.mark.parametrize("planned", [True, False])
+def test_prefill_output_only_16_byte_aligned(planned):
+    """An output whose rows start 16 bytes past a 32-byte boundary: the TMA
+    stores of whole-token rows and the threads' own stores of ragged rows give
+    the bytes of an aligned output."""
+    spec = dict(kind="prefill", dtype="bf16", B=3, Hq=16, Hkv=8, hd=128, P=16, chunks=[128, 77, 300],
+                prefixes=[0, 500, 64], norm=False, seed=77)
+    wl = synth.make_workload(spec)
+    run = GpuCase(wl, plan_prefill=planned)
+    n = wl.num_new_tokens
+    aligned = run.step()[:n].clone()
+    torch.cuda.synchronize()
+    shape = tuple(run.bufs.out.shape)
+    buf = torch.zeros(run.bufs.out.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(shape)
+    assert out.data_ptr() % 32 == 16
+    pa_prefill_varlen(run.desc, run.t["q"], run.t["cu_seqlens_q"], wl.batch, wl.max_new_len, n, run.k_cache,
+                      run.v_cache, run.t["block_tables"], wl.max_pages_per_seq, run.t["context_lens"],
+                      wl.max_context_len, wl.scale, out, run.bufs.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(out[:n].view(torch.int16), aligned.view(torch.int16))
+    assert torch.all(buf[:8].view(torch.int16) == 0)
+    assert pa_read_device_errors(reset=True) == 0
