@@ -365,3 +365,43 @@ def test_prefill_output_only_16_byte_aligned(planned):
     assert torch.equal(out[:n].view(torch.int16), aligned.view(torch.int16))
     assert torch.all(buf[:8].view(torch.int16) == 0)
     assert pa_read_device_errors(reset=True) == 0
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_prefill_step_never_reads_the_cache_before_the_write(graph):
+    """pa_prefill_step's planner starts beside the KV-write kernel; the
+    attention must still read the cache only after the write.  Before every
+    one of 20 steps the new tokens' cache slots are poisoned with NaN (a
+    kernel on the same stream): each step's output must equal the first one
+    bit for bit, eagerly and replayed from a CUDA graph."""
+    wl = synth.make_workload("qwen3_0p6b_chunked_prefill")
+    run = GpuCase(wl)
+    n = wl.num_new_tokens
+    ref = run.step()[:n].clone()
+    torch.cuda.synchronize()
+    slots = run.bufs.slots[:n].clone()
+    slots = slots[slots >= 0]
+    rows = wl.num_kv_heads * wl.head_dim
+    kc, vc = run.k_cache.view(-1, rows), run.v_cache.view(-1, rows)
+
+    def body():
+        kc.index_fill_(0, slots, float("nan"))
+        vc.index_fill_(0, slots, float("nan"))
+        run.step()
+
+    if graph:
+        body()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=s):
+            body()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+    for _ in range(20):
+        run.bufs.out.fill_(0)
+        g.replay() if graph else body()
+        torch.cuda.synchronize()
+        assert torch.equal(run.bufs.out[:n].view(torch.int16), ref.view(torch.int16))
+    assert pa_read_device_errors(reset=True) == 0
