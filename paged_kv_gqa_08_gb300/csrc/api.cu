@@ -95,6 +95,7 @@ cudaError_t current_device_info(DeviceInfo* out) {
       return e;
     if ((e = cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
     g_info[dev] = di;
   }
   *out = g_info[dev];

@@ -16,6 +16,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int max_smem_optin = 0;  // bytes per block with the opt-in attribute
   int cc_major = 0, cc_minor = 0;
+  int l2_bytes = 0;        // L2 cache size
 };
 // Properties of the current device (queried once per device).
 cudaError_t current_device_info(DeviceInfo* out);

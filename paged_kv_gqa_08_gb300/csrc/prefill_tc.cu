@@ -1237,6 +1237,7 @@ struct PlanParams {
   int4* splits;  // [split_cap] {request, pair, first slot, parts}
   int32_t* hdr;  // {units, split pairs, tau, pairs, work counter}
   int64_t num_tokens;
+  int64_t kv_block_tokens;  // context tokens whose K and V fill a third of L2 (0: order by cost alone)
   int32_t B, TQ, Hkv, n_sm, max_seqlen_q, cap_ctx, pair_cap, slot_cap, split_cap;
 };
 
@@ -1296,6 +1297,19 @@ PA_DEVINL int unit_cost(int len, int nq, int part) {
 }
 PA_DEVINL int cost_bucket(int len, int nq, int part) { return min(unit_cost(len, nq, part), kPlanBuckets - 1); }
 
+// Order of the units.  When the pairs fill more than kSplitWaves waves (no
+// split) and their requests' K and V do not fit in L2 together, the requests
+// are taken in blocks whose K and V fill about a third of L2, longest first
+// within a block: longest first over the whole batch would run every
+// request's pairs at once and read their K / V tiles back from DRAM several
+// times.  Buckets are handed out from the highest index down.
+constexpr int kMaxKvBlocks = 8;
+constexpr int kBlockBuckets = kPlanBuckets / kMaxKvBlocks;
+PA_DEVINL int order_bucket(int len, int nq, int part, int blk, bool blocked) {
+  return blocked ? (kMaxKvBlocks - 1 - blk) * kBlockBuckets + min(unit_cost(len, nq, part), kBlockBuckets - 1)
+                 : cost_bucket(len, nq, part);
+}
+
 // A pair of nt key tiles cut into `parts` ranges: the first nt % parts ranges
 // hold one tile more than the others (lengths base + 1 and base).
 template <bool kScore>
@@ -1312,8 +1326,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
   if (tid == 0) sh_max_nt = 0;
   for (int i = tid; i < kPlanBuckets; i += kPlanThreads) cursor[i] = 0;
 
-  // 1. the q-tile pairs of every request and their key-tile counts
-  unsigned long long carry = 0;
+  // 1. the q-tile pairs of every request and their key-tile counts; a pair's
+  //    .w holds its q-tiles with rows (bits 0-7) and its request's K/V block
+  //    (bits 8-15: context tokens of the requests before it / kv_block_tokens)
+  unsigned long long carry = 0, carry_l = 0;
   int max_nt = 0;
   for (int base = 0; base < q.B; base += kPlanThreads) {
     const int b = base + tid;
@@ -1330,16 +1346,24 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
       else
         np = ((n + q.TQ - 1) / q.TQ + 1) / 2;
     }
-    unsigned long long tot;
+    unsigned long long tot, tot_l;
     const unsigned long long off = carry + block_scan_excl<unsigned long long>(np, sh_scan, &tot);
+    const unsigned long long l_before =
+        carry_l + block_scan_excl<unsigned long long>(np > 0 ? static_cast<unsigned long long>(L) : 0ull, sh_scan,
+                                                      &tot_l);
+    const int blk = q.kv_block_tokens > 0
+                        ? static_cast<int>(min(l_before / static_cast<unsigned long long>(q.kv_block_tokens),
+                                               static_cast<unsigned long long>(kMaxKvBlocks - 1)))
+                        : 0;
     for (int k = 0; k < np; ++k) {
       const int nt = (L - n + min((2 * k + 2) * q.TQ, n) + kBN - 1) / kBN;
-      const int4 pr = make_int4(b, k, nt, (2 * k + 1) * q.TQ < n ? 2 : 1);
+      const int4 pr = make_int4(b, k, nt, ((2 * k + 1) * q.TQ < n ? 2 : 1) | (blk << 8));
       if (off + k < static_cast<unsigned long long>(q.pair_cap)) q.pairs[off + k] = pr;
       if (off + k < kPlanSmemPairs) sh_pairs[off + k] = pr;
       max_nt = max(max_nt, nt);
     }
     carry += tot;
+    carry_l += tot_l;
   }
   if (max_nt > 0) atomicMax(&sh_max_nt, max_nt);
   if (carry > static_cast<unsigned long long>(q.pair_cap)) {  // lengths disagree with the workspace's sizes
@@ -1351,6 +1375,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     return;
   }
   const int n_pairs = static_cast<int>(carry);
+  const bool blocked = q.kv_block_tokens > 0 && carry_l > static_cast<unsigned long long>(q.kv_block_tokens) &&
+                       static_cast<int64_t>(n_pairs) * q.Hkv > static_cast<int64_t>(kSplitWaves) * q.n_sm;
   cta_sync();
   max_nt = sh_max_nt;
   auto pair_at = [&](int i) -> int4 { return i < kPlanSmemPairs ? sh_pairs[i] : q.pairs[i]; };
@@ -1388,7 +1414,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     int slots = 0;
     for (int i = lane; i < n_pairs; i += 32) {
       const int4 pr = pair_at(i);
-      const int nt = pr.z, nq = pr.w;
+      const int nt = pr.z, nq = pr.w & 0xff;
       const int parts = div_near(nt + t_c - 1, t_c, inv_t);
       const int split = parts > 1;
       const int base = div_near(nt, parts, 1.f / parts), rem = nt - base * parts;
@@ -1491,10 +1517,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
   // 3. histogram of unit costs, then bucket cursors in descending cost order
   for (int i = tid; i < n_pairs; i += kPlanThreads) {
     const int4 pr = pair_at(i);
-    const int nt = pr.z, nq = pr.w;
+    const int nt = pr.z, nq = pr.w & 0xff, blk = pr.w >> 8;
     const int parts = parts_of(nt, tau), base = nt / parts, rem = nt - base * parts, split = parts > 1;
-    if (rem) atomicAdd(&cursor[cost_bucket(base + 1, nq, split)], rem);
-    if (parts > rem) atomicAdd(&cursor[cost_bucket(base, nq, split)], parts - rem);
+    if (rem) atomicAdd(&cursor[order_bucket(base + 1, nq, split, blk, blocked)], rem);
+    if (parts > rem) atomicAdd(&cursor[order_bucket(base, nq, split, blk, blocked)], parts - rem);
   }
   cta_sync();
   {
@@ -1528,8 +1554,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PlanPa
     if (parts > 0) {
       const int slot0 = static_cast<int>((before >> 32) & 0xffff), si = static_cast<int>(before >> 48);
       const int base = pr.z / parts, rem = pr.z - base * parts;
-      const int p_hi = rem ? atomicAdd(&cursor[cost_bucket(base + 1, pr.w, split)], rem) : 0;
-      const int p_lo = parts > rem ? atomicAdd(&cursor[cost_bucket(base, pr.w, split)], parts - rem) : 0;
+      const int nq = pr.w & 0xff, blk = pr.w >> 8;
+      const int p_hi = rem ? atomicAdd(&cursor[order_bucket(base + 1, nq, split, blk, blocked)], rem) : 0;
+      const int p_lo =
+          parts > rem ? atomicAdd(&cursor[order_bucket(base, nq, split, blk, blocked)], parts - rem) : 0;
       for (int k = 0; k < parts; ++k) {
         const int j0 = k * base + min(k, rem);
         const int j1 = j0 + base + (k < rem);
@@ -1801,6 +1829,13 @@ cudaError_t launch_prefill_tc(const pa_cache_desc& d, const PrefillArgs& a, cuda
   q.TQ = TQ;
   q.Hkv = d.num_kv_heads;
   q.n_sm = pl.n_sm;
+  {
+    // context tokens whose K and V (all kv-heads) fill a third of L2
+    DeviceInfo di;
+    if ((e = current_device_info(&di)) != cudaSuccess) return e;
+    const int64_t kv_per_token = static_cast<int64_t>(d.num_kv_heads) * 128 * 2 * 2;
+    q.kv_block_tokens = di.l2_bytes > 0 ? std::max<int64_t>(1, di.l2_bytes / 3 / kv_per_token) : 0;
+  }
   q.max_seqlen_q = a.max_seqlen_q;
   q.cap_ctx = static_cast<int32_t>(std::min<int64_t>(a.max_context_len, int64_t(a.max_pages) << p.log2P));
   q.pair_cap = pl.pair_cap;
