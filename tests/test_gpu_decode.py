@@ -47,6 +47,8 @@ SMALL = [
     ("bf16", 12, 2, 64, 16, [66, 500]),             # G = 6, head_dim 64
     ("f32", 14, 2, 64, 16, [20, 90]),               # G = 7
     ("f32", 24, 4, 128, 16, [64, 3]),               # G = 6, head_dim 128
+    ("bf16", 64, 8, 128, 16, [1, 333, 2000]),       # the largest head set: 8 kv-heads x G = 8
+    ("f32", 64, 8, 64, 32, [90, 7]),                # the same in fp32, head_dim 64
 ]
 
 

@@ -61,6 +61,8 @@ SMALL = [
     ("bf16", 8, 4, 64, 16, [20, 5], [40, 0], True),             # head_dim 64 (CUDA-core kernel)
     ("f32", 4, 2, 64, 16, [1, 9, 33], [0, 16, 5], True),
     ("f32", 8, 4, 128, 32, [70, 2], [0, 100], False),
+    ("bf16", 64, 8, 128, 16, [70, 5, 130], [33, 300, 0], True),   # the largest head set: 8 kv-heads x G = 8
+    ("bf16", 64, 8, 64, 16, [40, 3], [9, 120], False),             # the same with head_dim 64 (CUDA cores)
 ]
 
 
