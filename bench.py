@@ -718,8 +718,9 @@ def main():
     e2e_step_ms = e2e_ms / max(20, args.steps // 5)
     from paged_kv_gqa_08_gb300 import pa_decode_plan_info
     n_parts, _ = pa_decode_plan_info(d.desc, wl.batch, wl.max_context_len, 0)
-    # per step: decode plan, split-KV decode with the KV write, merge (if split)
-    launches = args.steps * (2 + (1 if n_parts > 1 else 0))
+    # per step: the split-KV decode with the KV write, the merge (if split), and a
+    # plan kernel before them beyond 512 requests (include/pagedattn.h, pa_decode)
+    launches = args.steps * (1 + (1 if n_parts > 1 else 0) + (1 if wl.batch > 512 else 0))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -226,7 +226,10 @@ PA_API pa_status pa_decode_plan_info(const pa_cache_desc* desc, int32_t batch, i
  * The keys of all requests are cut into equal shares, one per CTA; a request
  * spread over several CTAs gets per-share (o, log-sum-exp) partials that a
  * second kernel merges (split-KV).  Shares depend only on context_lens, so the
- * result is bitwise independent of which physical pages hold the keys.
+ * result is bitwise independent of which physical pages hold the keys.  Up to
+ * 512 requests every CTA computes the shares itself (the call launches the
+ * decode kernel and, when some request is split, the merge kernel); beyond,
+ * a one-CTA plan kernel computes them first.
  *
  *   q                [batch, num_q_heads, head_dim] contiguous.
  *   block_tables     int32 [batch, max_pages_per_seq].
