@@ -728,7 +728,7 @@ def main():
         "config": headline_config(wl, world),
         "attn_tok_per_s": tok_s,
         "hbm_frac_of_step": value / world / hbm_peak,
-        "roofline": {"kernel": "pa_decode_kv_write (plan + split-KV decode with KV write + merge kernels)",
+        "roofline": {"kernel": "pa_decode_kv_write (split-KV decode with the KV write, planned in-kernel, + merge)",
                      "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic, "peak_source": f"hbm_gbs of {peak_src}",
