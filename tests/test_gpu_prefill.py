@@ -407,3 +407,35 @@ def test_prefill_step_never_reads_the_cache_before_the_write(graph):
         torch.cuda.synchronize()
         assert torch.equal(run.bufs.out[:n].view(torch.int16), ref.view(torch.int16))
     assert pa_read_device_errors(reset=True) == 0
+
+
+@pytest.mark.parametrize("planned", [True, False])
+def test_prefill_step_with_a_padding_row_equals_the_separate_calls(planned):
+    """A padding row (context length 0) inside pa_prefill_step: its tokens get
+    position 0 and slot -1, its output rows stay untouched, no flag is raised,
+    and everything equals the separate calls bit for bit."""
+    spec = dict(kind="prefill", dtype="bf16", B=4, Hq=16, Hkv=8, hd=128, P=16, chunks=[40, 9, 130, 3],
+                prefixes=[100, 0, 257, 31], norm=True, seed=91)
+    wl = synth.make_workload(spec)
+    runs = [GpuCase(wl, plan_prefill=planned), GpuCase(wl, plan_prefill=planned)]
+    n = wl.num_new_tokens
+    pad = 1
+    outs = []
+    for k, run in enumerate(runs):
+        run.t["context_lens"][pad] = 0
+        run.bufs.out.fill_(7.0)
+        run.bufs.positions.fill_(-5)
+        run.bufs.slots.fill_(-5)
+        pa_read_device_errors(reset=True)
+        outs.append(run.step() if k == 0 else _separate_calls(run))
+        torch.cuda.synchronize()
+        assert pa_read_device_errors(reset=True) == 0
+    a, b = runs
+    s0, s1 = int(wl.cu_seqlens_q[pad]), int(wl.cu_seqlens_q[pad + 1])
+    assert torch.all(outs[0][s0:s1] == 7.0)
+    assert torch.all(a.bufs.positions[s0:s1] == 0) and torch.all(a.bufs.slots[s0:s1] == -1)
+    assert torch.equal(outs[0][:n].view(torch.int16), outs[1][:n].view(torch.int16))
+    assert torch.equal(a.bufs.positions[:n], b.bufs.positions[:n])
+    assert torch.equal(a.bufs.slots[:n], b.bufs.slots[:n])
+    assert torch.equal(a.k_cache.view(torch.int16), b.k_cache.view(torch.int16))
+    assert torch.equal(a.v_cache.view(torch.int16), b.v_cache.view(torch.int16))
